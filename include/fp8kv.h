@@ -1,0 +1,218 @@
+/*
+ * fp8kv.h -- C ABI of libfp8kv.so: calibrated-scale E4M3 FP8 paged KV-cache
+ * insertion and exact paged decode / speculative-verifier attention on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources (the "b70-optimization-lab" pages):
+ *  - "Laguna S 2.1 INT4 -- calibrated FP8 KV on Intel B70", section "Contract":
+ *    target KV is explicit E4M3 FP8 with one calibrated scalar K scale and one V
+ *    scale per layer; no runtime scale calculation.  Section "Initial
+ *    optimization order": profile the FP8 cache update and exact q1/M12 paged
+ *    attention separately; scaled E4M3 insertion at the Q/K norm + RoPE boundary.
+ *  - "Laguna S 2.1 KV-cache precision decision", section "What the official
+ *    checkpoint requests": kv_cache_scheme = static ("dynamic": false),
+ *    symmetric, per-tensor ("strategy": "tensor"), minmax observer; section
+ *    "BF16 versus FP8 in concrete terms": 8 KV heads x dim 128, 2048 B per token
+ *    per layer in FP8 vs 4096 B in BF16, "quantize, store FP8" on write and
+ *    "scale/dequantize" on read; 36 sliding-window-512 and 12 global layers.
+ *  - "Laguna FP8 KV -- replicated embedding win, page-32 build, and host
+ *    boundary", section "Page-32 attention experiment": page 32 and page 64,
+ *    global and sliding attention, and the rule that a fallback path
+ *    invalidates a result.
+ *  - "Laguna S 2.1 B70 campaign transfer ledger", table "Result progression",
+ *    row "Persistent attention metadata": fixed-address metadata refreshed in
+ *    place (here: every buffer is caller-owned; the library allocates no
+ *    memory).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked (device) are device pointers owned by the caller; they
+ *    must stay valid until the work queued on `stream` has finished.  Host
+ *    integers are sizes.  `stream` is a cudaStream_t (NULL = legacy default
+ *    stream); all work is queued asynchronously on it, nothing synchronises.
+ *  - Arguments are validated on the host before any launch.  A rejected call
+ *    returns a status below and launches nothing.  Shapes the kernels do not
+ *    implement return FP8KV_ERR_UNSUPPORTED: there is no slower fallback path.
+ *  - A failed launch returns FP8KV_ERR_CUDA (cudaGetLastError is consumed).
+ *  - Contents that the host cannot see (slot ids, positions, page ids,
+ *    sequence lengths) are checked on the device: an offending row is skipped
+ *    (never read or written out of bounds) and a bit is set in the device
+ *    status word, read with fp8kv_device_status().
+ *  - bf16 is the IEEE-like bfloat16 bit layout; every tensor is dense,
+ *    row-major, in the order of its dimension list, 16-byte aligned.
+ */
+#ifndef FP8KV_H
+#define FP8KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8KV_OK = 0,
+    FP8KV_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned, bad enum */
+    FP8KV_ERR_UNSUPPORTED = 2,  /* valid request outside the implemented shapes     */
+    FP8KV_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required       */
+    FP8KV_ERR_CUDA = 4          /* a CUDA runtime call or a launch failed           */
+} fp8kv_status;
+
+typedef enum {
+    FP8KV_CACHE_E4M3 = 0,       /* 1 byte per element, E4M3FN codes, scaled          */
+    FP8KV_CACHE_BF16 = 1        /* 2 bytes per element, stored as is, scales unused  */
+} fp8kv_cache_dtype;
+
+/* Device status bits (fp8kv_device_status). */
+#define FP8KV_DEV_BAD_SLOT      0x1u  /* slot_mapping entry >= num_pages*page_size   */
+#define FP8KV_DEV_BAD_POSITION  0x2u  /* position outside [0, max_pos)              */
+#define FP8KV_DEV_BAD_SEQ_LEN   0x4u  /* seq_len < M or beyond the block-table row  */
+#define FP8KV_DEV_WAIT_TIMEOUT  0x8u  /* a bounded pipeline wait gave up            */
+
+/*
+ * fp8kv_cache_insert -- write T new tokens into the paged K and V caches.
+ *
+ * Operation ("KV-cache precision decision", property table row "Cache
+ * write/read work": quantize, store FP8; scales per "Contract"): for every
+ * token t with slot s = slot_mapping[t] >= 0, head h, element d:
+ *     E4M3:  cache[s / page_size][h][s % page_size][d] =
+ *                e4m3_rne_satfinite( fp32(x[t][h][d]) / scale )
+ *     BF16:  cache[...] = x[t][h][d]  (bits copied, scales ignored, may be NULL)
+ * with fp32 IEEE division, round to nearest even, saturation to +-448
+ * (infinities included), NaN -> 0x7F with the input's sign, -0 -> 0x80.
+ * Slots < 0 are skipped; slots not named are left untouched.  Duplicate
+ * non-negative slots race (unspecified which token wins).
+ *
+ *   k, v          (device) bf16 [T][Hkv][D]
+ *   slot_mapping  (device) int64 [T]
+ *   k_scale, v_scale (device) one fp32 each, > 0 (E4M3 only)
+ *   k_cache, v_cache (device) [num_pages][Hkv][page_size][D] of the cache dtype
+ *   D must be 128; page_size 32 or 64; T may be 0 (no launch).
+ * Device check: slot >= num_pages*page_size -> row skipped, FP8KV_DEV_BAD_SLOT.
+ */
+int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping, int T,
+                       int Hkv, int D, const float* k_scale, const float* v_scale,
+                       void* k_cache, void* v_cache, int num_pages, int page_size,
+                       int cache_dtype, void* stream);
+
+/*
+ * fp8kv_qk_norm_rope_insert -- the Q/K RMSNorm + RoPE boundary fused with the
+ * E4M3 insert ("calibrated FP8 KV on Intel B70", "Initial optimization order",
+ * item 3; ledger table "Result progression", row "Exact fusion stack").
+ *
+ * For each token t at position pos = positions[t] and each Q head and K head
+ * row x (D = 128), in fp32 with this fixed order (reproduced bit for bit):
+ *     part_l  = sum of squares of x[4l..4l+3] accumulated as
+ *               fma(x3,x3, fma(x2,x2, fma(x1,x1, x0*x0)))          l = 0..31
+ *     ss      = parts added pairwise: l + (l+16), then +8, +4, +2, +1
+ *     r       = 1 / sqrt(ss / 128 + eps)                (IEEE sqrt, divide)
+ *     y_i     = bf16( bf16(x_i * r) * w_i )
+ *     o_k     = bf16( fma(y_k,    c_k, -(y_k+64 * s_k)) )   k = 0..63
+ *     o_k+64  = bf16( fma(y_k+64, c_k,   y_k    * s_k ) )
+ * with c_k = cos_sin[pos][k], s_k = cos_sin[pos][64 + k].  Q rows go to q_out;
+ * rotated K rows and the raw V rows are inserted as in fp8kv_cache_insert
+ * (E4M3 cache only).
+ *
+ *   q (device) bf16 [T][Hq][D]; k, v (device) bf16 [T][Hkv][D]
+ *   positions (device) int64 [T]; q_norm_w, k_norm_w (device) bf16 [D]
+ *   cos_sin (device) fp32 [max_pos][D]: cos of the 64 frequencies, then sines
+ *   q_out (device) bf16 [T][Hq][D] (must not alias q)
+ *   other arguments as fp8kv_cache_insert.
+ * Device checks: position outside [0, max_pos) -> token skipped entirely
+ * (FP8KV_DEV_BAD_POSITION); bad slot -> K/V of that token skipped.
+ */
+int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const void* v,
+                              const int64_t* positions, const void* q_norm_w,
+                              const void* k_norm_w, float eps, const float* cos_sin,
+                              int max_pos, void* q_out, const int64_t* slot_mapping, int T,
+                              int Hq, int Hkv, int D, const float* k_scale,
+                              const float* v_scale, void* k_cache, void* v_cache,
+                              int num_pages, int page_size, void* stream);
+
+/*
+ * fp8kv_paged_attention_plan -- the split-KV partition fp8kv_paged_attention
+ * will use for these host-visible sizes on the current device.
+ *   split_tokens: 0 = choose automatically; otherwise a positive multiple of
+ *   page_size.  Returns FP8KV_OK and writes *num_splits (>= 1, the largest
+ *   number of partitions any sequence can have) and *split_tokens_out.
+ */
+int fp8kv_paged_attention_plan(int B, int M, int Hq, int Hkv, int D, int page_size,
+                               int max_seq_len, int window_left, int split_tokens,
+                               int* num_splits, int* split_tokens_out);
+
+/* Workspace bytes fp8kv_paged_attention needs for the same arguments
+ * (0 when one partition per sequence suffices; (size_t)-1 on bad arguments). */
+size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D,
+                                            int page_size, int max_seq_len, int window_left,
+                                            int split_tokens);
+
+/*
+ * fp8kv_paged_attention -- exact paged attention over the cache for M new
+ * query rows per sequence ("calibrated FP8 KV on Intel B70", "Initial
+ * optimization order", items 2 and 4; M = 1 is decode, M = 12 the width-12
+ * verifier of "Contract").
+ *
+ * Sequence b has L = seq_lens[b] tokens cached, the last M of them the new
+ * rows; row m sits at position p = L - M + m and query head h reads KV head
+ * h / (Hq/Hkv).  Key j is visible to row m iff j <= p and, when
+ * window_left >= 0, j >= p - window_left (a window of W keys including the
+ * row itself is window_left = W - 1).  Logical key j lives in physical page
+ * block_table[b][j / page_size] at offset j % page_size.  With
+ * Kd = decode(k_code) * k_scale, Vd = decode(v_code) * v_scale (BF16 cache:
+ * the stored values, scales unused):
+ *     out[b][m][h] = softmax_j( (q . Kd_j) * sm_scale ) . Vd      (rounded to bf16)
+ * computed with fp32 accumulation.  Long contexts are cut into partitions of
+ * split_tokens keys whose partial (max, sum, unnormalised output) are combined
+ * by a reduce kernel through their log-sum-exp.
+ *
+ *   q            (device) bf16 [B][M][Hq][D]
+ *   k_cache, v_cache (device) [num_pages][Hkv][page_size][D] (cache_dtype)
+ *   block_table  (device) int32 [B][max_pages_per_seq]; entries of pages with
+ *                no visible key are never read
+ *   seq_lens     (device) int32 [B]; max_seq_len (host) >= every seq_lens[b]
+ *   k_scale, v_scale (device) fp32 scalars (E4M3 only)
+ *   sm_scale     (host) fp32 logit multiplier, e.g. 1/sqrt(D)
+ *   window_left  (host) -1 for a global layer, else >= 0
+ *   split_tokens (host) 0 = automatic, else a multiple of page_size
+ *   workspace    (device) >= fp8kv_paged_attention_workspace_size(...) bytes,
+ *                may be NULL when that size is 0; contents need no
+ *                initialisation and are scratch after the call
+ *   out          (device) bf16 [B][M][Hq][D]
+ * Supported: D = 128, page_size 32 or 64, 1 <= M <= 16, Hq % Hkv == 0,
+ * M * (Hq/Hkv) <= 144.  B = 0 launches nothing.
+ * Device checks: seq_len < M, seq_len > max_seq_len or more pages than
+ * max_pages_per_seq -> that sequence's output is left untouched
+ * (FP8KV_DEV_BAD_SEQ_LEN); page ids outside [0, num_pages) read zeros.
+ */
+int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cache,
+                          int cache_dtype, const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq,
+                          int Hkv, int D, int page_size, int num_pages, const float* k_scale,
+                          const float* v_scale, float sm_scale, int window_left,
+                          int split_tokens, void* workspace, size_t workspace_bytes, void* out,
+                          void* stream);
+
+/*
+ * fp8kv_e4m3_encode_bits -- encode the fp32 bit patterns first .. first+n-1
+ * with the same device routine the insert kernels use (for exhaustive checks
+ * of the encoder).  out (device) uint8 [n].
+ */
+int fp8kv_e4m3_encode_bits(uint32_t first, size_t n, uint8_t* out, void* stream);
+
+/* Text of a status code (static storage). */
+const char* fp8kv_status_string(int status);
+
+/* Kernel variant and partition count chosen by the last fp8kv_paged_attention
+ * call on this host thread, as text (truncated to n-1 bytes).  Returns the
+ * full length. */
+int fp8kv_last_dispatch(char* buf, size_t n);
+
+/* Read (and with clear != 0, reset) the device status word of the current
+ * device.  Synchronises the device.  Returns FP8KV_OK or FP8KV_ERR_CUDA. */
+int fp8kv_device_status(unsigned int* status, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8KV_H */

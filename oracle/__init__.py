@@ -39,6 +39,7 @@ def _declare(L):
     L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     L.oracle_e4m3_encode_array.argtypes = [vp, sz, vp]
     L.oracle_e4m3_decode_array.argtypes = [vp, sz, vp]
+    L.oracle_e4m3_encode_bits_range.argtypes = [ctypes.c_uint32, sz, vp]
     L.oracle_cache_insert.restype = i32
     L.oracle_cache_insert.argtypes = [vp, vp, vp, i32, i32, i32, f32, f32, vp, vp, i32, i32, i32]
     L.oracle_rope_table.argtypes = [f64, i32, i32, vp]
@@ -67,6 +68,13 @@ def e4m3_encode(x):
     x = _c(x, np.float32)
     out = np.empty(x.shape, np.uint8)
     lib().oracle_e4m3_encode_array(_p(x), x.size, _p(out))
+    return out
+
+
+def e4m3_encode_bits(first, n):
+    """Codes of the fp32 bit patterns first .. first+n-1."""
+    out = np.empty(n, np.uint8)
+    lib().oracle_e4m3_encode_bits_range(first, n, _p(out))
     return out
 
 

@@ -436,3 +436,9 @@ int oracle_paged_attention(ATTN_PARAMS, double* out)
     free(rows);
     return rc;
 }
+
+/* Encode the fp32 bit patterns first .. first+n-1 (exhaustive encoder checks). */
+void oracle_e4m3_encode_bits_range(uint32_t first, size_t n, uint8_t* out)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(bits_f32(first + (uint32_t)i));
+}

@@ -1,0 +1,126 @@
+"""The C-ABI library builds, loads and exports every symbol include/fp8kv.h
+declares; host-side validation rejects bad arguments before any launch.
+No kernel runs here (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from verify_attention_gb300 import build, fp8kv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8kv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return fp8kv.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8kv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fp8kv_cache_insert", "fp8kv_qk_norm_rope_insert", "fp8kv_paged_attention",
+              "fp8kv_paged_attention_workspace_size", "fp8kv_paged_attention_plan",
+              "fp8kv_status_string", "fp8kv_last_dispatch", "fp8kv_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert fp8kv.fp8kv_status_string(0) == "ok"
+    assert "unsupported" in fp8kv.fp8kv_status_string(2)
+    assert "workspace" in fp8kv.fp8kv_status_string(3)
+    assert fp8kv.fp8kv_status_string(99) == "unknown status"
+
+
+NULL = ctypes.c_void_p(0)
+P16 = ctypes.c_void_p(1 << 20)          # fake, 16-byte aligned: never dereferenced
+
+
+def _attn(L, **over):
+    a = dict(q=P16, k=P16, v=P16, dt=0, bt=P16, mpps=4, sl=P16, maxL=100, B=1, M=1, Hq=72, Hkv=8, D=128,
+             ps=32, P=16, ks=P16, vs=P16, sm=0.088, wl=-1, split=32, ws=P16, wsb=1 << 30, out=P16,
+             stream=NULL)
+    a.update(over)
+    return L.fp8kv_paged_attention(*a.values())
+
+
+def test_attention_validation(L):
+    E_INV, E_UNS, E_WS = 1, 2, 3
+    assert _attn(L, q=NULL) == E_INV
+    assert _attn(L, D=64) == E_UNS
+    assert _attn(L, ps=16, split=0) == E_UNS
+    assert _attn(L, M=17) == E_UNS
+    assert _attn(L, M=0) == E_INV
+    assert _attn(L, Hq=70) == E_INV                 # not a multiple of Hkv
+    assert _attn(L, M=16, Hq=80) == E_UNS           # 16 x 10 rows > 144
+    assert _attn(L, split=48) == E_INV              # not a multiple of the page size
+    assert _attn(L, maxL=200) == E_INV              # beyond max_pages_per_seq * page_size
+    assert _attn(L, dt=7) == E_INV
+    assert _attn(L, ks=NULL) == E_INV
+    assert _attn(L, q=ctypes.c_void_p((1 << 20) + 8)) == E_INV   # misaligned
+    assert _attn(L, ws=NULL) == E_WS
+    assert _attn(L, wsb=16) == E_WS
+    assert _attn(L, wl=-2) == E_INV
+
+
+def test_insert_validation(L):
+    f = L.fp8kv_cache_insert
+    args = [P16, P16, P16, 4, 8, 128, P16, P16, P16, P16, 16, 32, 0, NULL]
+    bad = list(args); bad[0] = NULL
+    assert f(*bad) == 1
+    bad = list(args); bad[5] = 96
+    assert f(*bad) == 2
+    bad = list(args); bad[11] = 48
+    assert f(*bad) == 2
+    bad = list(args); bad[12] = 5
+    assert f(*bad) == 1
+    bad = list(args); bad[6] = NULL
+    assert f(*bad) == 1
+    bad = list(args); bad[3] = 0                    # T = 0: nothing to do
+    assert f(*bad) == 0
+    g = L.fp8kv_qk_norm_rope_insert
+    a2 = [P16, P16, P16, P16, P16, P16, 1e-6, P16, 100, ctypes.c_void_p(2 << 20), P16, 4, 72, 8, 128, P16,
+          P16, P16, P16, 16, 32, NULL]
+    bad = list(a2); bad[9] = P16                    # q_out aliases q
+    assert g(*bad) == 1
+    bad = list(a2); bad[6] = -1.0
+    assert g(*bad) == 1
+    bad = list(a2); bad[14] = 64
+    assert g(*bad) == 2
+
+
+def test_plan_and_workspace_host_logic(L):
+    # explicit partitions: 131072 keys of page 64 in partitions of 2048 keys
+    ns, st = fp8kv.fp8kv_paged_attention_plan(1, 1, 72, 8, 128, 64, 131072, -1, 2048)
+    assert (ns, st) == (64, 2048)
+    assert fp8kv.fp8kv_paged_attention_workspace_size(1, 1, 72, 8, 128, 64, 131072, -1, 2048) == \
+        1 * 1 * 72 * 64 * 130 * 4
+    # one partition: no workspace
+    assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 4096) == 0
+    # a window of 512 with 12 rows spans at most ceil(523/64)+1 = 10 pages of 64
+    ns, st = fp8kv.fp8kv_paged_attention_plan(1, 12, 72, 8, 128, 64, 8192, 511, 64)
+    assert ns == 10
+    with pytest.raises(fp8kv.Fp8kvError):
+        fp8kv.fp8kv_paged_attention_plan(1, 1, 72, 8, 128, 64, 1000, -1, 100)
+
+
+def test_binding_rejects_cpu_tensors():
+    k = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fp8kv.fp8kv_cache_insert(k, k, torch.zeros(1, dtype=torch.int64), None, None,
+                                 torch.zeros(1, 8, 32, 128, dtype=torch.uint8),
+                                 torch.zeros(1, 8, 32, 128, dtype=torch.uint8))

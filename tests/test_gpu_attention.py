@@ -1,0 +1,172 @@
+"""GPU parity of paged attention against the float64 oracle, within
+|err| <= 1e-2 + 1e-2 |ref|.  All calls go through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from verify_attention_gb300 import build, inputs as gen
+from tests.helpers import (assert_close, gpu_attention, gpu_caches, oracle_attention, oracle_caches,
+                           sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    from verify_attention_gb300 import fp8kv
+    fp8kv.fp8kv_device_status(clear=True)
+    yield
+    assert fp8kv.fp8kv_device_status(clear=True) == 0
+
+
+def fp8kv():
+    from verify_attention_gb300 import fp8kv as f
+    return f
+
+
+def run_case(case, split_tokens=0, cache_dtype="e4m3", poison=0xA5, rows=None):
+    kc, vc, ks, vs = gpu_caches(case, cache_dtype, poison=poison)
+    out = gpu_attention(case, kc, vc, ks, vs, split_tokens=split_tokens)
+    torch.cuda.synchronize()
+    okc, ovc = oracle_caches(case, cache_dtype, poison=poison)
+    if rows is None:
+        ref = oracle_attention(case, okc, ovc, cache_dtype=cache_dtype)
+        return out, ref, assert_close(out, ref, f"split={split_tokens}")
+    ref = oracle_attention(case, okc, ovc, rows=rows, cache_dtype=cache_dtype)
+    o = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
+    return out, ref, assert_close(o, ref, f"split={split_tokens}")
+
+
+SMALL = [
+    # seq_lens, M, ps, window, Hq, Hkv
+    ([1, 77, 300], 1, 32, None, 72, 8),
+    ([1, 77, 300], 1, 64, None, 72, 8),
+    ([12, 500], 12, 64, None, 72, 8),
+    ([12, 500], 12, 64, 64, 72, 8),
+    ([130, 33], 12, 32, 40, 72, 8),
+    ([200], 16, 32, None, 72, 8),            # 144 rows: nine row tiles
+    ([95, 260], 2, 64, None, 72, 8),         # 18 rows: two row tiles, two key groups
+    ([61, 300], 5, 32, 100, 72, 8),          # 45 rows: three row tiles
+    ([257, 64], 3, 32, 65, 18, 2),           # the pages' per-rank shape, sliding (64, 0)
+    ([257, 64], 3, 32, None, 18, 2),         # same, global (-1, -1)
+    ([40], 7, 64, None, 8, 8),               # no GQA grouping
+]
+
+
+@pytest.mark.parametrize("seq_lens,M,ps,window,Hq,Hkv", SMALL)
+@pytest.mark.parametrize("split_tokens", [0, 64])
+def test_attention_small_shapes(seq_lens, M, ps, window, Hq, Hkv, split_tokens):
+    case = gen.layer_case(8000 + sum(seq_lens) + M, seq_lens, M, ps, window=window, Hq=Hq, Hkv=Hkv)
+    run_case(case, split_tokens=split_tokens)
+
+
+@pytest.mark.parametrize("M,ps", [(1, 64), (12, 32)])
+def test_attention_bf16_cache(M, ps):
+    case = gen.layer_case(8100 + M, [333, 70], M, ps, window=None)
+    run_case(case, split_tokens=0, cache_dtype="bf16")
+    run_case(case, split_tokens=ps * 2, cache_dtype="bf16")
+
+
+def test_attention_stale_nan_slots_do_not_leak():
+    """Unwritten slots hold the E4M3 NaN code; keys outside every row's range
+    must not contribute (0 * NaN)."""
+    case = gen.layer_case(8200, [45, 100], 12, 32, window=20)
+    out, ref, _ = run_case(case, poison=0x7F)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_attention_page_permutation_bit_identical():
+    case = gen.layer_case(8300, [700, 129], 12, 64, window=None)
+    kc, vc, ks, vs = gpu_caches(case)
+    out = gpu_attention(case, kc, vc, ks, vs)
+    perm = torch.randperm(kc.shape[0], generator=gen.generator(1)).cuda()
+    inv = torch.argsort(perm)
+    bt = case.layout.block_table
+    bt2 = torch.where(bt >= 0, inv.cpu()[bt.clamp(min=0).long()].to(torch.int32), bt)
+    case2 = gen.LayerCase(**{**case.__dict__, "layout": gen.PagedLayout(case.layout.page_size,
+                                                                         case.layout.num_pages, bt2,
+                                                                         case.layout.seq_lens)})
+    out2 = gpu_attention(case2, kc[perm].contiguous(), vc[perm].contiguous(), ks, vs)
+    assert torch.equal(out, out2)
+
+
+def test_attention_split_agrees_with_unsplit():
+    case = gen.layer_case(8400, [3000], 1, 64)
+    kc, vc, ks, vs = gpu_caches(case)
+    a = gpu_attention(case, kc, vc, ks, vs, split_tokens=3008 // 64 * 64 + 64).float()
+    for st in (64, 256, 1024):
+        b = gpu_attention(case, kc, vc, ks, vs, split_tokens=st).float()
+        assert (a - b).abs().max().item() <= 1e-2
+
+
+def test_attention_unvisited_pages_never_read():
+    """Block-table entries of pages before every window are -1 (and so would
+    read zeros if touched): the result must not change."""
+    case = gen.layer_case(8500, [900], 12, 32, window=100)
+    kc, vc, ks, vs = gpu_caches(case)
+    out = gpu_attention(case, kc, vc, ks, vs)
+    bt = case.layout.block_table.clone()
+    first = (900 - 12 - 99) // 32
+    bt[0, :first] = -1
+    case.layout.block_table = bt
+    out2 = gpu_attention(case, kc, vc, ks, vs)
+    assert torch.equal(out, out2)
+
+
+def test_attention_bad_seq_len_flagged():
+    f = fp8kv()
+    case = gen.layer_case(8600, [100], 12, 32)
+    kc, vc, ks, vs = gpu_caches(case)
+    case.layout.seq_lens[0] = 5                     # fewer than M = 12
+    f.fp8kv_device_status(clear=True)
+    gpu_attention(case, kc, vc, ks, vs, max_seq_len=100)
+    assert f.fp8kv_device_status(clear=True) & f.DEV_BAD_SEQ_LEN
+    case.layout.seq_lens[0] = 101                   # beyond the host's max_seq_len
+    gpu_attention(case, kc, vc, ks, vs, max_seq_len=100)
+    assert f.fp8kv_device_status(clear=True) & f.DEV_BAD_SEQ_LEN
+
+
+def test_dispatch_marker_reports_variant():
+    case = gen.layer_case(8700, [2000], 1, 64)
+    kc, vc, ks, vs = gpu_caches(case)
+    gpu_attention(case, kc, vc, ks, vs, split_tokens=512)
+    d = fp8kv().fp8kv_last_dispatch()
+    assert "ps=64" in d and "e4m3" in d and "splits=4" in d
+
+
+# ------------------------------------------------------------ the configs
+
+def test_cfg1_tiny_decode():
+    run_case(gen.cfg1_case())
+
+
+@pytest.mark.parametrize("window", [None, 512])
+def test_cfg2_single_layer_verify(window):
+    run_case(gen.cfg2_case(window))
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+@pytest.mark.parametrize("layer", [0, 3])        # sliding, global
+def test_cfg3_verify_layers(layer, ps):
+    case = gen.cfg3_case(layer, ps)
+    rows = None if layer == 0 else sample_rows(1, 12, 72, 96, seed=layer)
+    run_case(case, rows=rows)
+
+
+@pytest.mark.parametrize("split_tokens", [2048, 0])
+def test_cfg4_long_context_decode_full_size(split_tokens):
+    case = gen.cfg4_case(0)
+    run_case(case, split_tokens=split_tokens)
+
+
+def test_cfg4_bf16_cache_full_size():
+    case = gen.cfg4_case(1)
+    run_case(case, split_tokens=2048, cache_dtype="bf16", rows=sample_rows(1, 1, 72, 24, seed=4))
+
+
+@pytest.mark.parametrize("layer", [0, 1])        # global, sliding
+def test_cfg5_serving_mix_full_size_sampled(layer):
+    case = gen.cfg5_case(layer)
+    rows = sample_rows(64, 12, 72, 48, seed=layer)
+    run_case(case, rows=rows)

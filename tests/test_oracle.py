@@ -117,6 +117,12 @@ def test_encode_vs_brute_force_grid_search():
     assert np.array_equal(oracle.e4m3_encode(x), _brute_force_encode(x))
 
 
+def test_encode_bits_range_matches_array_encoder():
+    first = 0x3F7F0000
+    x = (np.arange(1 << 16, dtype=np.uint32) + np.uint32(first)).view(np.float32)
+    assert np.array_equal(oracle.e4m3_encode_bits(first, 1 << 16), oracle.e4m3_encode(x))
+
+
 def test_encode_vs_torch_cast_in_range():
     rng = np.random.default_rng(6)
     x = (rng.standard_normal(100000) * 50).astype(np.float32)

@@ -1,0 +1,769 @@
+// attention.cu -- exact paged decode / verifier attention over the FP8 (or
+// BF16) KV cache, with split-KV partials and a log-sum-exp reduce kernel.
+//
+// Method: "exact q1/M12 paged attention" over the E4M3 cache with calibrated
+// per-tensor scales ("Laguna S 2.1 INT4 -- calibrated FP8 KV on Intel B70",
+// sections "Contract" and "Initial optimization order"); "scale/dequantize"
+// on read ("Laguna S 2.1 KV-cache precision decision", property table); global
+// and sliding-window layers, GQA with 8 KV heads of dimension 128 (same page,
+// "BF16 versus FP8 in concrete terms"); page sizes 32 and 64 ("Laguna FP8 KV --
+// replicated embedding win, page-32 build, and host boundary", section
+// "Page-32 attention experiment").
+//
+// Kernel shape (one CTA per (partition, KV head, sequence)):
+//  * a producer warp streams the (page, head) tiles of K and V -- each a
+//    contiguous page_size x 128 block of the [page][head][slot][dim] cache --
+//    into a ring of shared-memory stages with 3-D TMA loads (128-byte swizzle,
+//    so the fragment reads below are bank-conflict free);
+//  * consumer warps own 16 query rows each (the M x G rows of one KV head,
+//    padded to 16) and run Q.K^T and P.V on the tensor cores (m16n8k16,
+//    fp32 accumulate).  E4M3 codes are widened to f16 in registers (exact) and
+//    Q is scaled by a per-row power of two into f16 range (exact for bf16);
+//    the BF16 cache runs the same loop in bf16;
+//  * online softmax in fp32 (log2 domain) with quad shuffles;
+//  * when the M x G rows fit one row tile (decode), up to four key groups of
+//    warps split the pages of a partition and are merged through shared
+//    memory at the end;
+//  * one partition per sequence writes bf16 output directly; otherwise each
+//    partition writes (max, sum, unnormalised output) and attn_reduce_kernel
+//    combines them.
+#include <stdio.h>
+
+#include "common.cuh"
+
+namespace fp8kv {
+
+int status_attention(unsigned int* s, int clear) { return read_status(s, clear); }
+
+constexpr int kMaxRowTiles = 9;          // M*G <= 144
+constexpr int kStageBudget = 96 * 1024;  // bytes of K/V stages per CTA
+
+struct AttnParams {
+    const uint16_t* q;          // bf16 [B][M][Hq][128]
+    const int32_t* block_table; // [B][mpps]
+    const int32_t* seq_lens;    // [B]
+    const float* k_scale;
+    const float* v_scale;
+    float* ws_o;                // [B*M*Hq][num_splits][128]
+    float* ws_ml;               // [B*M*Hq][num_splits][2]
+    uint16_t* out;              // bf16 [B][M][Hq][128]
+    float sm_scale;
+    int mpps, B, M, Hq, Hkv, G, R, NT, KW, SG;   // SG: stages per key group
+    int window_left, split_pages, num_splits, page_size, max_seq_len;
+};
+
+template <int PS, bool FP8>
+struct Cfg {
+    static constexpr int kElem = FP8 ? 1 : 2;
+    static constexpr int kTileBytes = PS * 128 * kElem;          // one (page, head) tile
+    static constexpr int kStageBytes = 2 * kTileBytes;           // K + V
+    static constexpr int kStages = kStageBudget / kStageBytes;   // 12 / 6 / 6 / 3
+    static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+// Visible key range of query row r (M*G rows per KV head, row = m*G + g).
+struct RowPos {
+    int p, lo;
+};
+__device__ __forceinline__ RowPos row_pos(int r, int R, int G, int L, int M, int wl) {
+    if (r >= R) r = R - 1;                       // padding rows mirror the last row
+    const int m = r / G;
+    RowPos rp;
+    rp.p = L - M + m;
+    rp.lo = (wl >= 0) ? max(0, rp.p - wl) : 0;
+    return rp;
+}
+
+// Smem byte offset of 16-byte chunk `ch` of row `row` in a 128-byte-swizzled tile.
+__device__ __forceinline__ uint32_t swz(int row, int ch) { return row * 128 + (((ch ^ row) & 7) << 4); }
+
+template <int PS, bool FP8>
+__global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
+    using C = Cfg<PS, FP8>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = (uint64_t*)(smem + S * C::kStageBytes);   // full[S], empty[S]
+
+    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_cons = P.NT * P.KW;
+    const int L = P.seq_lens[b];
+    if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
+        if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+        return;
+    }
+    const int lo0 = (P.window_left >= 0) ? max(0, L - P.M - P.window_left) : 0;
+    const int first_page = lo0 / PS, last_page = (L - 1) / PS;
+    const int nsplit_b = (last_page - first_page + P.split_pages) / P.split_pages;
+    if (nsplit_b > P.num_splits) {   // cannot happen when L <= max_seq_len; never index past the plan
+        if (threadIdx.x == 0 && split == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+        return;
+    }
+    if (split >= nsplit_b) return;
+    const int page_begin = first_page + split * P.split_pages;
+    const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
+
+    // Each key group owns SG consecutive stages.  Page i of this partition goes
+    // to group i % KW, its j-th page (j = i / KW) to stage g*SG + j % SG, use
+    // j / SG of that stage: every wait below is for the next phase of a barrier
+    // only its own consumer advances, so a parity test can never pass early.
+    const int SG = P.SG;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);
+            mbar_init(smem_u32(&bars[S + s]), P.NT);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == n_cons) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        const uint64_t policy = policy_evict_first();
+        const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
+        bool ok = true;
+        int issued = 0;
+        for (int base = 0; base < n_pages && ok; base += 32) {
+            const int mine = (base + lane < n_pages) ? bt[base + lane] : 0;
+            const int cnt = min(32, n_pages - base);
+            for (int j = 0; j < cnt; ++j) {
+                const int phys = __shfl_sync(0xffffffffu, mine, j);
+                const int i = base + j;
+                const int jj = i / P.KW, use = jj / SG;
+                const int s = (i % P.KW) * SG + jj % SG;
+                if (lane == 0) {
+                    if (use > 0) ok = mbar_wait(smem_u32(&bars[S + s]), (use - 1) & 1);
+                    if (ok) {
+                        const uint32_t full = smem_u32(&bars[s]);
+                        const uint32_t dk = smem_u32(smem + s * C::kStageBytes);
+                        const uint32_t dv = dk + C::kTileBytes;
+                        mbar_expect_tx(full, C::kStageBytes);
+                        if (FP8) {
+                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                        } else {
+                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dk + PS * 128, &tm_k, 64, hk * PS, phys, full, policy);
+                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++issued;
+            }
+        }
+        // Do not leave while copies into this CTA's shared memory are in flight.
+        if (lane == 0) {
+            for (int i = max(0, issued - P.KW * SG); i < issued; ++i) {
+                const int jj = i / P.KW;
+                mbar_wait(smem_u32(&bars[(i % P.KW) * SG + jj % SG]), (jj / SG) & 1);
+            }
+        }
+        return;
+    }
+    if (warp > n_cons) return;
+
+    // --------------------------------------------------------------- consumer
+    const int rt = warp % P.NT, kg = warp / P.NT;
+    const int g = lane >> 2, c = lane & 3;
+    const int r0 = rt * 16 + g, r1 = r0 + 8;
+    const RowPos rp0 = row_pos(r0, P.R, P.G, L, P.M, P.window_left);
+    const RowPos rp1 = row_pos(r1, P.R, P.G, L, P.M, P.window_left);
+
+    // Q fragments (A operand, 8 k-steps).  k-slot -> head-dim mapping:
+    //   FP8 : k-step ks of thread c covers dims 32c + 4ks + {0,1 | 2,3}
+    //   BF16: dims 16c + 4ks (ks < 4) or 64 + 16c + 4(ks-4)
+    uint32_t qa[8][4];
+    float mult[2];
+    {
+        float qf[2][32];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = hr ? r1 : r0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) qf[hr][j] = 0.f;
+            if (r < P.R) {
+                const int m = r / P.G, hq = hk * P.G + r % P.G;
+                const uint4* src = (const uint4*)(P.q + (((int64_t)b * P.M + m) * P.Hq + hq) * 128);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int vec = FP8 ? (4 * c + u) : (u < 2 ? 2 * c + u : 8 + 2 * c + (u - 2));
+                    const uint4 w = src[vec];
+                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        qf[hr][8 * u + 2 * e] = bf16_lo(ww[e]);
+                        qf[hr][8 * u + 2 * e + 1] = bf16_hi(ww[e]);
+                    }
+                }
+            }
+        }
+        const float log2e = 1.4426950408889634f;
+        if (FP8) {
+            const float ks = *P.k_scale;
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float amax = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(qf[hr][j]));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                // power-of-two prescale putting the row maximum in [2^14, 2^15)
+                int e = 14;
+                const uint32_t ab = __float_as_uint(amax);
+                if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
+                    const int be = (int)((ab >> 23) & 0xff);
+                    e = be ? be - 127 : -127;
+                }
+                const int sh = max(-100, min(100, 14 - e));
+                const float scale = ldexpf(1.0f, sh);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) qf[hr][j] *= scale;
+                mult[hr] = ks * P.sm_scale * log2e * ldexpf(1.0f, -sh);
+            }
+#pragma unroll
+            for (int ks2 = 0; ks2 < 8; ++ks2) {
+                qa[ks2][0] = pack_f16x2(qf[0][4 * ks2], qf[0][4 * ks2 + 1]);
+                qa[ks2][1] = pack_f16x2(qf[1][4 * ks2], qf[1][4 * ks2 + 1]);
+                qa[ks2][2] = pack_f16x2(qf[0][4 * ks2 + 2], qf[0][4 * ks2 + 3]);
+                qa[ks2][3] = pack_f16x2(qf[1][4 * ks2 + 2], qf[1][4 * ks2 + 3]);
+            }
+        } else {
+            mult[0] = mult[1] = P.sm_scale * log2e;
+#pragma unroll
+            for (int ks2 = 0; ks2 < 8; ++ks2) {
+                qa[ks2][0] = pack_bf16x2(qf[0][4 * ks2], qf[0][4 * ks2 + 1]);
+                qa[ks2][1] = pack_bf16x2(qf[1][4 * ks2], qf[1][4 * ks2 + 1]);
+                qa[ks2][2] = pack_bf16x2(qf[0][4 * ks2 + 2], qf[0][4 * ks2 + 3]);
+                qa[ks2][3] = pack_bf16x2(qf[1][4 * ks2 + 2], qf[1][4 * ks2 + 3]);
+            }
+        }
+    }
+
+    // warp-uniform bounds used to skip masking on interior chunks
+    int pmin = min(rp0.p, rp1.p), lomax = max(rp0.lo, rp1.lo);
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+        pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, off));
+        lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, off));
+    }
+
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+    bool ok = true;
+
+    for (int i = kg; i < n_pages; i += P.KW) {
+        const int jj = i / P.KW;
+        const int s = kg * SG + jj % SG;
+        ok = mbar_wait(smem_u32(&bars[s]), (jj / SG) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const uint8_t* kt = smem + s * C::kStageBytes;
+        const uint8_t* vt = kt + C::kTileBytes;
+        const int kpage = (page_begin + i) * PS;
+
+#pragma unroll 1
+        for (int ch32 = 0; ch32 < PS / 32; ++ch32) {
+            const int kfirst = kpage + 32 * ch32;
+            // ---- S = Q K^T for 32 keys (4 n-tiles of 8 keys)
+            float sacc[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+                const int row = 32 * ch32 + 8 * nt + g;
+                if (FP8) {
+                    const uint4 k0 = *(const uint4*)(kt + swz(row, 2 * c));
+                    const uint4 k1 = *(const uint4*)(kt + swz(row, 2 * c + 1));
+                    const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+                    for (int ks2 = 0; ks2 < 8; ++ks2)
+                        mma_f16(sacc[nt], qa[ks2], e4m3x2_to_f16x2(kw[ks2]), e4m3x2_to_f16x2(kw[ks2] >> 16));
+                } else {
+                    const uint4 k0 = *(const uint4*)(kt + swz(row, 2 * c));
+                    const uint4 k1 = *(const uint4*)(kt + swz(row, 2 * c + 1));
+                    const uint4 k2 = *(const uint4*)(kt + PS * 128 + swz(row, 2 * c));
+                    const uint4 k3 = *(const uint4*)(kt + PS * 128 + swz(row, 2 * c + 1));
+                    mma_bf16(sacc[nt], qa[0], k0.x, k0.y);
+                    mma_bf16(sacc[nt], qa[1], k0.z, k0.w);
+                    mma_bf16(sacc[nt], qa[2], k1.x, k1.y);
+                    mma_bf16(sacc[nt], qa[3], k1.z, k1.w);
+                    mma_bf16(sacc[nt], qa[4], k2.x, k2.y);
+                    mma_bf16(sacc[nt], qa[5], k2.z, k2.w);
+                    mma_bf16(sacc[nt], qa[6], k3.x, k3.y);
+                    mma_bf16(sacc[nt], qa[7], k3.z, k3.w);
+                }
+            }
+            // ---- scale to log2 units, mask, online softmax
+            const bool need_mask = (kfirst + 31 > pmin) || (kfirst < lomax);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float t = sacc[nt][e] * mult[e >> 1];
+                    if (need_mask) {
+                        const int key = kfirst + 8 * nt + 2 * c + (e & 1);
+                        const RowPos& rp = (e >> 1) ? rp1 : rp0;
+                        if (key > rp.p || key < rp.lo) t = -INFINITY;
+                    }
+                    sacc[nt][e] = t;
+                }
+            }
+            float alpha[2];
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                float tmax = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) tmax = fmaxf(tmax, fmaxf(sacc[nt][2 * hr], sacc[nt][2 * hr + 1]));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+                tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+                const float mnew = fmaxf(mrow[hr], tmax);
+                const float mref = (mnew == -INFINITY) ? 0.f : mnew;
+                alpha[hr] = ex2(mrow[hr] - mref);
+                mrow[hr] = mnew;
+                float sum = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    sacc[nt][2 * hr] = ex2(sacc[nt][2 * hr] - mref);
+                    sacc[nt][2 * hr + 1] = ex2(sacc[nt][2 * hr + 1] - mref);
+                    sum += sacc[nt][2 * hr] + sacc[nt][2 * hr + 1];
+                }
+                lrow[hr] = lrow[hr] * alpha[hr] + sum;
+            }
+            if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    o[i2][0] *= alpha[0];
+                    o[i2][1] *= alpha[0];
+                    o[i2][2] *= alpha[1];
+                    o[i2][3] *= alpha[1];
+                }
+            }
+            // ---- O += P V  (2 k-steps of 16 keys)
+            // keys outside every row's range (past the sequence end, or before
+            // the first window) contribute exact zeros even if stale data there
+            // is not finite
+            const bool zero_v = (kfirst + 31 >= L) || (kfirst < lo0);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
+                uint32_t pa[4];
+                if (FP8) {
+                    pa[0] = pack_f16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
+                    pa[1] = pack_f16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
+                    pa[2] = pack_f16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+                    pa[3] = pack_f16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+                } else {
+                    pa[0] = pack_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
+                    pa[1] = pack_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
+                    pa[2] = pack_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+                    pa[3] = pack_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+                }
+                const int rA = 32 * ch32 + 16 * kk + 2 * c;   // keys rA, rA+1, rA+8, rA+9
+                bool kz[4] = {false, false, false, false};
+                if (zero_v) {
+                    const int key = kpage + rA;
+                    kz[0] = key >= L || key < lo0;
+                    kz[1] = key + 1 >= L || key + 1 < lo0;
+                    kz[2] = key + 8 >= L || key + 8 < lo0;
+                    kz[3] = key + 9 >= L || key + 9 < lo0;
+                }
+                if (FP8) {
+#pragma unroll
+                    for (int T = 0; T < 4; ++T) {
+                        const int chk = 2 * T + (g >> 2), wofs = (g & 3) * 4;
+                        uint32_t w0 = *(const uint32_t*)(vt + swz(rA, chk) + wofs);
+                        uint32_t w1 = *(const uint32_t*)(vt + swz(rA + 1, chk) + wofs);
+                        uint32_t w8 = *(const uint32_t*)(vt + swz(rA + 8, chk) + wofs);
+                        uint32_t w9 = *(const uint32_t*)(vt + swz(rA + 9, chk) + wofs);
+                        if (kz[0]) w0 = 0;
+                        if (kz[1]) w1 = 0;
+                        if (kz[2]) w8 = 0;
+                        if (kz[3]) w9 = 0;
+                        const uint32_t a01 = prmt(w0, w1, 0x5140), b01 = prmt(w0, w1, 0x7362);
+                        const uint32_t a89 = prmt(w8, w9, 0x5140), b89 = prmt(w8, w9, 0x7362);
+                        mma_f16(o[4 * T + 0], pa, e4m3x2_to_f16x2(a01), e4m3x2_to_f16x2(a89));
+                        mma_f16(o[4 * T + 1], pa, e4m3x2_to_f16x2(a01 >> 16), e4m3x2_to_f16x2(a89 >> 16));
+                        mma_f16(o[4 * T + 2], pa, e4m3x2_to_f16x2(b01), e4m3x2_to_f16x2(b89));
+                        mma_f16(o[4 * T + 3], pa, e4m3x2_to_f16x2(b01 >> 16), e4m3x2_to_f16x2(b89 >> 16));
+                    }
+                } else {
+#pragma unroll
+                    for (int T = 0; T < 8; ++T) {
+                        const uint8_t* vh = vt + (T >> 2) * PS * 128;
+                        const int chk = 2 * (T & 3) + (g >> 2), wofs = (g & 3) * 4;
+                        uint32_t w0 = *(const uint32_t*)(vh + swz(rA, chk) + wofs);
+                        uint32_t w1 = *(const uint32_t*)(vh + swz(rA + 1, chk) + wofs);
+                        uint32_t w8 = *(const uint32_t*)(vh + swz(rA + 8, chk) + wofs);
+                        uint32_t w9 = *(const uint32_t*)(vh + swz(rA + 9, chk) + wofs);
+                        if (kz[0]) w0 = 0;
+                        if (kz[1]) w1 = 0;
+                        if (kz[2]) w8 = 0;
+                        if (kz[3]) w9 = 0;
+                        mma_bf16(o[2 * T + 0], pa, prmt(w0, w1, 0x5410), prmt(w8, w9, 0x5410));
+                        mma_bf16(o[2 * T + 1], pa, prmt(w0, w1, 0x7632), prmt(w8, w9, 0x7632));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars[S + s]));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    // all consumers are done with the stages (every issued copy was consumed),
+    // so the ring is reused as the merge area: per (key group, row) 128 floats
+    // of O, then m and l.
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 1);
+        lrow[hr] += __shfl_xor_sync(0xffffffffu, lrow[hr], 2);
+    }
+    constexpr int kRowStride = 132;   // floats
+    float* mergef = (float*)smem;
+    const int rows_pad = P.NT * 16;
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+        const int r = hr ? r1 : r0;
+        float* dst = mergef + ((int64_t)kg * rows_pad + r) * kRowStride;
+        if (FP8) {
+#pragma unroll
+            for (int T = 0; T < 4; ++T) {
+                // n-tile 4T+i, column n -> dim 32T + 4n + i; this thread has n = 2c, 2c+1
+                float4 lo4 = make_float4(o[4 * T + 0][2 * hr], o[4 * T + 1][2 * hr], o[4 * T + 2][2 * hr],
+                                         o[4 * T + 3][2 * hr]);
+                float4 hi4 = make_float4(o[4 * T + 0][2 * hr + 1], o[4 * T + 1][2 * hr + 1],
+                                         o[4 * T + 2][2 * hr + 1], o[4 * T + 3][2 * hr + 1]);
+                *(float4*)(dst + 32 * T + 8 * c) = lo4;
+                *(float4*)(dst + 32 * T + 8 * c + 4) = hi4;
+            }
+        } else {
+#pragma unroll
+            for (int T = 0; T < 8; ++T) {
+                // n-tile 2T+i, column n -> dim 16T + 2n + i
+                *(float4*)(dst + 16 * T + 4 * c) = make_float4(o[2 * T][2 * hr], o[2 * T + 1][2 * hr],
+                                                               o[2 * T][2 * hr + 1], o[2 * T + 1][2 * hr + 1]);
+            }
+        }
+        if (c == 0) {
+            dst[128] = mrow[hr];
+            dst[129] = lrow[hr];
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
+    if (!ok) return;
+
+    const float vs = FP8 ? *P.v_scale : 1.0f;
+    const int tid = threadIdx.x;
+    for (int item = tid; item < P.R * 32; item += n_cons * 32) {
+        const int r = item >> 5, d4 = (item & 31) * 4;
+        float mstar = -INFINITY;
+        for (int k2 = 0; k2 < P.KW; ++k2) mstar = fmaxf(mstar, mergef[((int64_t)k2 * rows_pad + r) * kRowStride + 128]);
+        float l = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (mstar != -INFINITY) {
+            for (int k2 = 0; k2 < P.KW; ++k2) {
+                const float* src = mergef + ((int64_t)k2 * rows_pad + r) * kRowStride;
+                const float w = ex2(src[128] - mstar);
+                l += w * src[129];
+                const float4 v4 = *(const float4*)(src + d4);
+                acc.x += w * v4.x;
+                acc.y += w * v4.y;
+                acc.z += w * v4.z;
+                acc.w += w * v4.w;
+            }
+        }
+        const int m = r / P.G, hq = hk * P.G + r % P.G;
+        const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hq;
+        if (nsplit_b == 1) {
+            const float f = vs / l;
+            *(uint2*)(P.out + row_idx * 128 + d4) =
+                make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
+        } else {
+            float* wo = P.ws_o + (row_idx * P.num_splits + split) * 128 + d4;
+            *(float4*)wo = make_float4(acc.x * vs, acc.y * vs, acc.z * vs, acc.w * vs);
+            if (d4 == 0) {
+                P.ws_ml[(row_idx * P.num_splits + split) * 2] = mstar;
+                P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l;
+            }
+        }
+    }
+}
+
+// One warp per output row (b, m, h): combine the partitions through their
+// log-sum-exp, O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p.
+__global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restrict__ ws_o,
+                                                          const float* __restrict__ ws_ml,
+                                                          const int32_t* __restrict__ seq_lens, int B, int M,
+                                                          int Hq, int mpps, int page_size, int window_left,
+                                                          int split_pages, int num_splits, int max_seq_len,
+                                                          uint16_t* out) {
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= (int64_t)B * M * Hq) return;
+    const int b = (int)(row / ((int64_t)M * Hq));
+    const int L = seq_lens[b];
+    if (L < M || L > max_seq_len || (L + page_size - 1) / page_size > mpps) return;
+    const int lo0 = (window_left >= 0) ? max(0, L - M - window_left) : 0;
+    const int first_page = lo0 / page_size, last_page = (L - 1) / page_size;
+    const int ns = (last_page - first_page + split_pages) / split_pages;
+    if (ns <= 1 || ns > num_splits) return;
+    const float* ml = ws_ml + row * num_splits * 2;
+    float mstar = -INFINITY;
+    for (int s = lane; s < ns; s += 32) mstar = fmaxf(mstar, ml[2 * s]);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* po = ws_o + row * num_splits * 128 + lane * 4;
+    for (int s = 0; s < ns; ++s) {
+        const float ms = ml[2 * s];
+        if (ms == -INFINITY) continue;
+        const float w = ex2(ms - mstar);
+        den += w * ml[2 * s + 1];
+        const float4 v4 = *(const float4*)(po + (int64_t)s * 128);
+        acc.x += w * v4.x;
+        acc.y += w * v4.y;
+        acc.z += w * v4.z;
+        acc.w += w * v4.w;
+    }
+    const float f = 1.0f / den;
+    *(uint2*)(out + row * 128 + lane * 4) =
+        make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
+}
+
+}  // namespace fp8kv
+
+// =====================================================================  host
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <set>
+#include <utility>
+
+#include <mutex>
+
+namespace fp8kv {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    });
+    return fn;
+}
+
+// 3-D view of a [num_pages][Hkv][PS][128] cache: x = element within the row,
+// y = head * PS + slot, z = page.  One box is one (page, head) tile (bf16 rows
+// are fetched as two 64-element boxes so each box row is 128 bytes).
+static bool make_cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int num_pages) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t elem = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {128, (cuuint64_t)Hkv * PS, (cuuint64_t)num_pages};
+    cuuint64_t strides[2] = {128 * elem, (cuuint64_t)Hkv * PS * 128 * elem};
+    cuuint32_t box[3] = {fp8 ? 128u : 64u, (cuuint32_t)PS, 1u};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int split_pages, num_splits, split_tokens;
+};
+
+static int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+static int check_sizes(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_len, int window_left,
+                       int split_tokens) {
+    if (B < 0 || M < 1 || Hq <= 0 || Hkv <= 0 || max_seq_len < 0 || window_left < -1 || split_tokens < 0)
+        return FP8KV_ERR_INVALID_ARG;
+    if (Hq % Hkv) return FP8KV_ERR_INVALID_ARG;
+    if (D != 128 || (PS != 32 && PS != 64) || M > 16) return FP8KV_ERR_UNSUPPORTED;
+    if (M * (Hq / Hkv) > 16 * kMaxRowTiles) return FP8KV_ERR_UNSUPPORTED;
+    if (split_tokens % PS) return FP8KV_ERR_INVALID_ARG;
+    if (B > 65535 || Hkv > 65535) return FP8KV_ERR_UNSUPPORTED;
+    return FP8KV_OK;
+}
+
+static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_len, int window_left,
+                     int split_tokens, Plan* p) {
+    int rc = check_sizes(B, M, Hq, Hkv, D, PS, max_seq_len, window_left, split_tokens);
+    if (rc) return rc;
+    // pages spanned by the visible keys of the longest sequence
+    int pages = ceil_div(max(max_seq_len, 1), PS);
+    if (window_left >= 0) pages = min(pages, ceil_div((int64_t)M + window_left, PS) + 1);
+    int sp;
+    if (split_tokens > 0) {
+        sp = split_tokens / PS;
+    } else {
+        // about four waves of two CTAs per SM over all (sequence, head)
+        // units, with at least 256 keys per partition
+        const int64_t units = (int64_t)max(B, 1) * Hkv;
+        const int64_t target = 8LL * num_sms();
+        const int per = (int)std::max<int64_t>(1, (target + units - 1) / units);
+        sp = max(ceil_div(pages, per), 256 / PS);
+    }
+    sp = max(1, min(sp, pages));
+    p->split_pages = sp;
+    p->num_splits = ceil_div(pages, sp);
+    p->split_tokens = sp * PS;
+    return FP8KV_OK;
+}
+
+static size_t ws_bytes(int B, int M, int Hq, const Plan& p) {
+    if (p.num_splits <= 1) return 0;
+    return (size_t)B * M * Hq * p.num_splits * (128 + 2) * sizeof(float);
+}
+
+// Opt in to the kernel's dynamic shared memory once per device (so that calls
+// made under CUDA-graph capture issue no attribute change).
+static int ensure_smem(const void* kern, int bytes) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void*>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8KV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({dev, kern})) return FP8KV_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return FP8KV_ERR_CUDA;
+    done.insert({dev, kern});
+    return FP8KV_OK;
+}
+
+template <int PS, bool FP8>
+static int launch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
+    using C = Cfg<PS, FP8>;
+    auto kern = paged_attention_kernel<PS, FP8>;
+    if (ensure_smem((const void*)kern, C::kSmem)) return FP8KV_ERR_CUDA;
+    dim3 grid(P.num_splits, P.Hkv, P.B);
+    kern<<<grid, (P.NT * P.KW + 1) * 32, C::kSmem, s>>>(tk, tv, P);
+    return launch_status();
+}
+
+}  // namespace fp8kv
+
+using namespace fp8kv;
+
+extern "C" int fp8kv_paged_attention_plan(int B, int M, int Hq, int Hkv, int D, int page_size,
+                                          int max_seq_len, int window_left, int split_tokens,
+                                          int* num_splits, int* split_tokens_out) {
+    Plan p;
+    int rc = make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &p);
+    if (rc) return rc;
+    if (num_splits) *num_splits = p.num_splits;
+    if (split_tokens_out) *split_tokens_out = p.split_tokens;
+    return FP8KV_OK;
+}
+
+extern "C" size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D, int page_size,
+                                                       int max_seq_len, int window_left, int split_tokens) {
+    Plan p;
+    if (make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &p)) return (size_t)-1;
+    return ws_bytes(B, M, Hq, p);
+}
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cache, int cache_dtype,
+                                     const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                     int max_seq_len, int B, int M, int Hq, int Hkv, int D, int page_size,
+                                     int num_pages, const float* k_scale, const float* v_scale, float sm_scale,
+                                     int window_left, int split_tokens, void* workspace, size_t workspace_bytes,
+                                     void* out, void* stream) {
+    if (cache_dtype != FP8KV_CACHE_E4M3 && cache_dtype != FP8KV_CACHE_BF16) return FP8KV_ERR_INVALID_ARG;
+    const bool fp8 = cache_dtype == FP8KV_CACHE_E4M3;
+    Plan plan;
+    int rc = make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &plan);
+    if (rc) return rc;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
+    if (fp8 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID_ARG;
+    if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(out)) return FP8KV_ERR_INVALID_ARG;
+    if (num_pages <= 0 || max_pages_per_seq <= 0) return FP8KV_ERR_INVALID_ARG;
+    if (max_seq_len < M || (int64_t)max_seq_len > (int64_t)max_pages_per_seq * page_size)
+        return FP8KV_ERR_INVALID_ARG;
+    if (!(sm_scale == sm_scale)) return FP8KV_ERR_INVALID_ARG;
+    const size_t need = ws_bytes(B, M, Hq, plan);
+    if (need && (!workspace || workspace_bytes < need || !al16(workspace))) return FP8KV_ERR_WORKSPACE;
+    if (B == 0) return FP8KV_OK;
+
+    CUtensorMap tk, tv;
+    if (!make_cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||
+        !make_cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
+        return FP8KV_ERR_CUDA;
+
+    AttnParams P;
+    P.q = (const uint16_t*)q;
+    P.block_table = block_table;
+    P.seq_lens = seq_lens;
+    P.k_scale = k_scale;
+    P.v_scale = v_scale;
+    P.ws_o = (float*)workspace;
+    P.ws_ml = need ? (float*)workspace + (size_t)B * M * Hq * plan.num_splits * 128 : nullptr;
+    P.out = (uint16_t*)out;
+    P.sm_scale = sm_scale;
+    P.mpps = max_pages_per_seq;
+    P.B = B;
+    P.M = M;
+    P.Hq = Hq;
+    P.Hkv = Hkv;
+    P.G = Hq / Hkv;
+    P.R = M * P.G;
+    P.NT = (P.R + 15) / 16;
+    {
+        // key groups split a partition's pages when one row tile leaves warps
+        // idle; each group keeps at least two stages in flight when it can
+        const int stages = page_size == 32 ? (fp8 ? Cfg<32, true>::kStages : Cfg<32, false>::kStages)
+                                           : (fp8 ? Cfg<64, true>::kStages : Cfg<64, false>::kStages);
+        int kw = P.NT == 1 ? 4 : (P.NT == 2 ? 2 : 1);
+        kw = std::max(1, std::min(kw, stages / 2));
+        P.KW = kw;
+        P.SG = stages / kw;
+    }
+    P.window_left = window_left;
+    P.split_pages = plan.split_pages;
+    P.num_splits = plan.num_splits;
+    P.page_size = page_size;
+    P.max_seq_len = max_seq_len;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    if (page_size == 32)
+        rc = fp8 ? launch<32, true>(tk, tv, P, s) : launch<32, false>(tk, tv, P, s);
+    else
+        rc = fp8 ? launch<64, true>(tk, tv, P, s) : launch<64, false>(tk, tv, P, s);
+    if (rc) return rc;
+    if (plan.num_splits > 1) {
+        const int64_t warps = (int64_t)B * M * Hq;
+        attn_reduce_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
+            P.ws_o, P.ws_ml, seq_lens, B, M, Hq, max_pages_per_seq, page_size, window_left, plan.split_pages,
+            plan.num_splits, max_seq_len, (uint16_t*)out);
+        rc = launch_status();
+        if (rc) return rc;
+    }
+    char buf[256];
+    snprintf(buf, sizeof buf,
+             "paged_attention_mma<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "
+             "split_tokens=%d grid=%dx%dx%d threads=%d reduce=%d",
+             page_size, fp8 ? "e4m3" : "bf16", P.R, P.NT, P.KW, P.SG, plan.num_splits, plan.split_tokens,
+             plan.num_splits, Hkv, B, (P.NT * P.KW + 1) * 32, plan.num_splits > 1 ? 1 : 0);
+    set_dispatch(buf);
+    return FP8KV_OK;
+}

@@ -1,0 +1,186 @@
+// common.cuh -- device helpers shared by the fp8kv kernels (sm_103a).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fp8kv.h"
+
+namespace fp8kv {
+
+// Device status word of this translation unit (bits FP8KV_DEV_*); each .cu
+// file has its own copy and a host reader, OR-ed by fp8kv_device_status.
+static __device__ unsigned int g_status;
+
+__device__ __forceinline__ void flag(unsigned int bits) { atomicOr(&g_status, bits); }
+
+// ------------------------------------------------------------------ E4M3
+
+// Two fp32 values -> two E4M3FN codes (lo in bits 0..7, hi in bits 8..15):
+// round to nearest even, saturating to +-448 (infinities included) by the
+// hardware conversion; NaN inputs become 0x7F with their own sign bit.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    uint32_t out = r;
+    uint32_t bl = __float_as_uint(lo), bh = __float_as_uint(hi);
+    if ((bl & 0x7fffffffu) > 0x7f800000u) out = (out & 0xff00u) | 0x7fu | ((bl >> 24) & 0x80u);
+    if ((bh & 0x7fffffffu) > 0x7f800000u) out = (out & 0x00ffu) | ((0x7fu | ((bh >> 24) & 0x80u)) << 8);
+    return out;
+}
+
+// Two E4M3 codes (bits 0..15) -> f16x2, exact (every E4M3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+    uint32_t r;
+    uint16_t c = (uint16_t)codes;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// 2^x on the special-function unit (the hardware ex2 instruction).
+__device__ __forceinline__ float ex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// ------------------------------------------------------------ tensor core
+
+// D += A * B, m16n8k16, fp32 accumulate; A row-major, B column-major.
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// ------------------------------------------------------ mbarrier and TMA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase with parity `phase` of an mbarrier to complete.  Gives up
+// after ~2 s of wall time (sets FP8KV_DEV_WAIT_TIMEOUT and returns false) so a
+// broken pipeline can never hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    if (ok) return true;
+    const uint64_t start = globaltimer();
+    while (true) {
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(bar), "r"(phase)
+            : "memory");
+        if (ok) return true;
+        if (globaltimer() - start > 2000000000ull) {
+            flag(FP8KV_DEV_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tm), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
+}
+
+}  // namespace fp8kv
+
+// Host-side helpers (api.cu).
+namespace fp8kv {
+int launch_status();                    // FP8KV_OK or FP8KV_ERR_CUDA after a launch
+int num_sms();                          // SM count of the current device
+void set_dispatch(const char* text);    // per-thread record of the last dispatch
+int status_insert(unsigned int* s, int clear);     // insert.cu
+int status_attention(unsigned int* s, int clear);  // attention.cu
+
+// OR this translation unit's status word into *s, optionally clearing it.
+static inline int read_status(unsigned int* s, int clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return FP8KV_ERR_CUDA;
+    if (clear) {
+        const unsigned int z = 0;
+        if (cudaMemcpyToSymbol(g_status, &z, sizeof(z)) != cudaSuccess) return FP8KV_ERR_CUDA;
+    }
+    *s |= v;
+    return FP8KV_OK;
+}
+}  // namespace fp8kv

@@ -1,0 +1,197 @@
+"""Thin ctypes binding of libfp8kv.so (include/fp8kv.h), same names as the C ABI.
+
+Only argument marshalling happens here: tensors become device pointers and
+sizes, the current torch stream becomes the cudaStream_t, and a non-zero
+status raises ``Fp8kvError``.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback: if the library is missing, the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfp8kv.so")
+
+FP8KV_CACHE_E4M3 = 0
+FP8KV_CACHE_BF16 = 1
+DEV_BAD_SLOT, DEV_BAD_POSITION, DEV_BAD_SEQ_LEN, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+
+_lib = None
+
+
+class Fp8kvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: status {status} ({fp8kv_status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m verify_attention_gb300.build` (nvcc, sm_103a)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, u32, f32, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_float,
+                                 ctypes.c_size_t)
+        L.fp8kv_cache_insert.restype = i32
+        L.fp8kv_cache_insert.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.fp8kv_qk_norm_rope_insert.restype = i32
+        L.fp8kv_qk_norm_rope_insert.argtypes = [vp, vp, vp, vp, vp, vp, f32, vp, i32, vp, vp, i32, i32,
+                                                i32, i32, vp, vp, vp, vp, i32, i32, vp]
+        L.fp8kv_paged_attention_plan.restype = i32
+        L.fp8kv_paged_attention_plan.argtypes = [i32] * 9 + [ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        L.fp8kv_paged_attention_workspace_size.restype = sz
+        L.fp8kv_paged_attention_workspace_size.argtypes = [i32] * 9
+        L.fp8kv_paged_attention.restype = i32
+        L.fp8kv_paged_attention.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32,
+                                            i32, i32, vp, vp, f32, i32, i32, vp, sz, vp, vp]
+        L.fp8kv_e4m3_encode_bits.restype = i32
+        L.fp8kv_e4m3_encode_bits.argtypes = [u32, sz, vp, vp]
+        L.fp8kv_status_string.restype = ctypes.c_char_p
+        L.fp8kv_status_string.argtypes = [i32]
+        L.fp8kv_last_dispatch.restype = i32
+        L.fp8kv_last_dispatch.argtypes = [ctypes.c_char_p, sz]
+        L.fp8kv_device_status.restype = i32
+        L.fp8kv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
+        _lib = L
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(fn, rc):
+    if rc != 0:
+        raise Fp8kvError(fn, rc)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _cache_dtype(cache: torch.Tensor) -> int:
+    if cache.dtype == torch.uint8:
+        return FP8KV_CACHE_E4M3
+    if cache.dtype == torch.bfloat16:
+        return FP8KV_CACHE_BF16
+    raise ValueError("cache must be uint8 (E4M3 codes) or bfloat16")
+
+
+def fp8kv_status_string(status: int) -> str:
+    return lib().fp8kv_status_string(status).decode()
+
+
+def fp8kv_cache_insert(k, v, slot_mapping, k_scale, v_scale, k_cache, v_cache, stream=None):
+    """k, v bf16 [T][Hkv][D]; slot_mapping int64 [T]; scales fp32 [1] (E4M3 only);
+    caches [num_pages][Hkv][page_size][D] uint8 (E4M3) or bf16."""
+    dt = _cache_dtype(k_cache)
+    _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16)
+    _dev(slot_mapping, "slot_mapping", torch.int64), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
+    T, Hkv, D = k.shape
+    num_pages, _, page_size, _ = k_cache.shape
+    rc = lib().fp8kv_cache_insert(_ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, _ptr(k_scale),
+                                  _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), num_pages, page_size,
+                                  dt, _stream(stream))
+    _check("fp8kv_cache_insert", rc)
+
+
+def fp8kv_qk_norm_rope_insert(q, k, v, positions, q_norm_w, k_norm_w, eps, cos_sin, q_out,
+                              slot_mapping, k_scale, v_scale, k_cache, v_cache, stream=None):
+    """Fused Q/K RMSNorm + RoPE + E4M3 insert; writes q_out (bf16 [T][Hq][D])."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (q_out, "q_out"), (q_norm_w, "q_norm_w"),
+                 (k_norm_w, "k_norm_w")):
+        _dev(t, n, torch.bfloat16)
+    _dev(positions, "positions", torch.int64), _dev(slot_mapping, "slot_mapping", torch.int64)
+    _dev(cos_sin, "cos_sin", torch.float32), _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    num_pages, _, page_size, _ = k_cache.shape
+    rc = lib().fp8kv_qk_norm_rope_insert(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(positions), _ptr(q_norm_w), _ptr(k_norm_w), float(eps),
+        _ptr(cos_sin), cos_sin.shape[0], _ptr(q_out), _ptr(slot_mapping), T, Hq, Hkv, D, _ptr(k_scale),
+        _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), num_pages, page_size, _stream(stream))
+    _check("fp8kv_qk_norm_rope_insert", rc)
+
+
+def fp8kv_paged_attention_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens=0):
+    ns, st = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().fp8kv_paged_attention_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                          split_tokens, ctypes.byref(ns), ctypes.byref(st))
+    _check("fp8kv_paged_attention_plan", rc)
+    return ns.value, st.value
+
+
+def fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                         split_tokens=0) -> int:
+    n = lib().fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len,
+                                                   window_left, split_tokens)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("fp8kv_paged_attention_workspace_size: bad arguments")
+    return n
+
+
+def fp8kv_paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale,
+                          sm_scale, window_left=-1, split_tokens=0, workspace=None, out=None,
+                          num_pages=None, stream=None):
+    """q bf16 [B][M][Hq][D]; caches [num_pages][Hkv][page_size][D]; block_table int32
+    [B][max_pages_per_seq]; seq_lens int32 [B] (context incl. the M new rows).
+    Returns out bf16 [B][M][Hq][D].  ``workspace`` (uint8 CUDA tensor) is
+    allocated by torch here when not given and needed."""
+    dt = _cache_dtype(k_cache)
+    _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
+    _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
+    B, M, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_cache.shape
+    if num_pages is None:
+        num_pages = P
+    need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                                split_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().fp8kv_paged_attention(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), int(max_seq_len), B, M, Hq, Hkv, D, page_size, int(num_pages), _ptr(k_scale),
+        _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
+    _check("fp8kv_paged_attention", rc)
+    return out
+
+
+def fp8kv_e4m3_encode_bits(first: int, n: int, out: torch.Tensor, stream=None):
+    _dev(out, "out", torch.uint8)
+    rc = lib().fp8kv_e4m3_encode_bits(first, n, _ptr(out), _stream(stream))
+    _check("fp8kv_e4m3_encode_bits", rc)
+
+
+def fp8kv_last_dispatch() -> str:
+    buf = ctypes.create_string_buffer(512)
+    lib().fp8kv_last_dispatch(buf, 512)
+    return buf.value.decode()
+
+
+def fp8kv_device_status(clear: bool = False) -> int:
+    s = ctypes.c_uint(0)
+    _check("fp8kv_device_status", lib().fp8kv_device_status(ctypes.byref(s), int(clear)))
+    return s.value
