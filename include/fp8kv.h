@@ -193,6 +193,38 @@ int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cach
                           void* stream);
 
 /*
+ * fp8kv_paged_attention_noalloc -- fp8kv_paged_attention without a
+ * caller-provided workspace.  (The pages have no counterpart: this is an
+ * integration convenience, not part of the method.)
+ *
+ * For callers that cannot allocate device memory where they run attention
+ * (an allocator-free serving loop, a fully carved-up memory pool, host code
+ * holding only a raw stream): the split-KV partials go to a buffer that is a
+ * file-scope __device__ array of FP8KV_NOALLOC_WORKSPACE_BYTES (32 MiB) inside
+ * the library.  Every GPU that loads the library holds that buffer until the
+ * process exits.  The call allocates nothing (no cudaMalloc, no allocating
+ * library routine).
+ *
+ * Arguments and results are those of fp8kv_paged_attention without
+ * workspace / workspace_bytes.  Requests whose workspace size
+ * (fp8kv_paged_attention_workspace_size) exceeds 32 MiB return
+ * FP8KV_ERR_WORKSPACE (a larger split_tokens needs less; otherwise use the
+ * allocating entry point).  The first call on a device looks up the buffer's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call shares the one buffer, which keeps
+ * the last call's contents (no part of it needs to start at zero): calls
+ * that overlap on the GPU -- on different streams, or from several threads --
+ * race and must be serialised by the caller.
+ */
+int fp8kv_paged_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                  int cache_dtype, const int32_t* block_table,
+                                  int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                  int B, int M, int Hq, int Hkv, int D, int page_size,
+                                  int num_pages, const float* k_scale, const float* v_scale,
+                                  float sm_scale, int window_left, int split_tokens, void* out,
+                                  void* stream);
+
+/*
  * fp8kv_e4m3_encode_bits -- encode the fp32 bit patterns first .. first+n-1
  * with the same device routine the insert kernels use (for exhaustive checks
  * of the encoder).  out (device) uint8 [n].

@@ -767,3 +767,60 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     set_dispatch(buf);
     return FP8KV_OK;
 }
+
+// ================================================ allocation-free variant
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: code inside an allocator-free serving loop, callers with a
+// memory pool that is already fully carved up, or host code that only has a
+// raw stream and no allocator handle.  For them this entry point uses a
+// file-scope device buffer as the split-KV workspace instead of a
+// caller-provided one.  The buffer is fixed at load time, so every GPU that
+// loads this library holds it until the process exits.
+
+#define FP8KV_NOALLOC_WORKSPACE_BYTES (32u << 20)
+
+static __device__ __align__(256) uint8_t g_noalloc_workspace[FP8KV_NOALLOC_WORKSPACE_BYTES];
+
+// Device address of g_noalloc_workspace, looked up once per device with that
+// device current (in host code the symbol is only a host-side stand-in).
+static int noalloc_workspace(void** ptr) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FP8KV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return FP8KV_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    return FP8KV_OK;
+}
+
+extern "C" int fp8kv_paged_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                             int cache_dtype, const int32_t* block_table, int max_pages_per_seq,
+                                             const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq,
+                                             int Hkv, int D, int page_size, int num_pages, const float* k_scale,
+                                             const float* v_scale, float sm_scale, int window_left,
+                                             int split_tokens, void* out, void* stream) {
+    const size_t need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len,
+                                                             window_left, split_tokens);
+    if (need == (size_t)-1) {
+        // same validation and status as the allocating entry point
+        return fp8kv_paged_attention(q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq, seq_lens,
+                                     max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale,
+                                     sm_scale, window_left, split_tokens, nullptr, 0, out, stream);
+    }
+    if (need > FP8KV_NOALLOC_WORKSPACE_BYTES) return FP8KV_ERR_WORKSPACE;
+    void* ws = nullptr;
+    if (need) {
+        const int rc = noalloc_workspace(&ws);
+        if (rc) return rc;
+    }
+    return fp8kv_paged_attention(q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq, seq_lens,
+                                 max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, sm_scale,
+                                 window_left, split_tokens, ws, need ? FP8KV_NOALLOC_WORKSPACE_BYTES : 0, out,
+                                 stream);
+}

@@ -51,6 +51,9 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_paged_attention.restype = i32
         L.fp8kv_paged_attention.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                             i32, i32, vp, vp, f32, i32, i32, vp, sz, vp, vp]
+        L.fp8kv_paged_attention_noalloc.restype = i32
+        L.fp8kv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                                                    i32, i32, i32, vp, vp, f32, i32, i32, vp, vp]
         L.fp8kv_e4m3_encode_bits.restype = i32
         L.fp8kv_e4m3_encode_bits.argtypes = [u32, sz, vp, vp]
         L.fp8kv_status_string.restype = ctypes.c_char_p
@@ -176,6 +179,26 @@ def fp8kv_paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_le
         _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
         workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
     _check("fp8kv_paged_attention", rc)
+    return out
+
+
+def fp8kv_paged_attention_noalloc(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale,
+                                  sm_scale, out, window_left=-1, split_tokens=0, num_pages=None, stream=None):
+    """fp8kv_paged_attention with the library's own fixed device workspace, for
+    callers that cannot allocate device memory: ``out`` must be given, nothing
+    is allocated here or in the library."""
+    dt = _cache_dtype(k_cache)
+    _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
+    _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(out, "out", torch.bfloat16)
+    B, M, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_cache.shape
+    rc = lib().fp8kv_paged_attention_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        int(max_seq_len), B, M, Hq, Hkv, D, page_size, int(P if num_pages is None else num_pages),
+        _ptr(k_scale), _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(out),
+        _stream(stream))
+    _check("fp8kv_paged_attention_noalloc", rc)
     return out
 
 
