@@ -4,6 +4,7 @@
 #include <mutex>
 #include <vector>
 
+#include "attention.cuh"
 #include "common.cuh"
 
 namespace fp8kv {
@@ -59,7 +60,9 @@ extern "C" int fp8kv_device_status(unsigned int* status, int clear) {
     if (!status) return FP8KV_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return FP8KV_ERR_CUDA;
     unsigned int s = 0;
-    if (fp8kv::status_insert(&s, clear) || fp8kv::status_attention(&s, clear)) return FP8KV_ERR_CUDA;
+    if (fp8kv::status_insert(&s, clear) || fp8kv::status_attention(&s, clear) ||
+        fp8kv::status_attention_tc(&s, clear))
+        return FP8KV_ERR_CUDA;
     *status = s;
     return FP8KV_OK;
 }

@@ -29,6 +29,7 @@
 //    combines them.
 #include <stdio.h>
 
+#include "attention.cuh"
 #include "common.cuh"
 
 namespace fp8kv {
@@ -37,20 +38,6 @@ int status_attention(unsigned int* s, int clear) { return read_status(s, clear);
 
 constexpr int kMaxRowTiles = 9;          // M*G <= 144
 constexpr int kStageBudget = 96 * 1024;  // bytes of K/V stages per CTA
-
-struct AttnParams {
-    const uint16_t* q;          // bf16 [B][M][Hq][128]
-    const int32_t* block_table; // [B][mpps]
-    const int32_t* seq_lens;    // [B]
-    const float* k_scale;
-    const float* v_scale;
-    float* ws_o;                // [B*M*Hq][num_splits][128]
-    float* ws_ml;               // [B*M*Hq][num_splits][2]
-    uint16_t* out;              // bf16 [B][M][Hq][128]
-    float sm_scale;
-    int mpps, B, M, Hq, Hkv, G, R, NT, KW, SG;   // SG: stages per key group
-    int window_left, split_pages, num_splits, page_size, max_seq_len;
-};
 
 template <int PS, bool FP8>
 struct Cfg {
@@ -516,6 +503,7 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     const int first_page = lo0 / page_size, last_page = (L - 1) / page_size;
     const int ns = (last_page - first_page + split_pages) / split_pages;
     if (ns <= 1 || ns > num_splits) return;
+    // partition weights: lane j owns partitions j, j+32, ...
     const float* ml = ws_ml + row * num_splits * 2;
     float mstar = -INFINITY;
     for (int s = lane; s < ns; s += 32) mstar = fmaxf(mstar, ml[2 * s]);
@@ -524,17 +512,40 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     float den = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* po = ws_o + row * num_splits * 128 + lane * 4;
-    for (int s = 0; s < ns; ++s) {
-        const float ms = ml[2 * s];
-        if (ms == -INFINITY) continue;
-        const float w = ex2(ms - mstar);
-        den += w * ml[2 * s + 1];
-        const float4 v4 = *(const float4*)(po + (int64_t)s * 128);
-        acc.x += w * v4.x;
-        acc.y += w * v4.y;
-        acc.z += w * v4.z;
-        acc.w += w * v4.w;
+    for (int base = 0; base < ns; base += 32) {
+        const int s_l = base + lane;
+        float w_l = 0.f;
+        if (s_l < ns) {
+            const float ms = ml[2 * s_l];
+            w_l = (ms == -INFINITY) ? 0.f : ex2(ms - mstar);
+            den += w_l * ml[2 * s_l + 1];
+        }
+        const int cnt = min(32, ns - base);
+        int j = 0;
+        for (; j + 4 <= cnt; j += 4) {         // four partial rows in flight
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) v[u] = *(const float4*)(po + (int64_t)(base + j + u) * 128);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float w = __shfl_sync(0xffffffffu, w_l, j + u);
+                acc.x += w * v[u].x;
+                acc.y += w * v[u].y;
+                acc.z += w * v[u].z;
+                acc.w += w * v[u].w;
+            }
+        }
+        for (; j < cnt; ++j) {
+            const float w = __shfl_sync(0xffffffffu, w_l, j);
+            const float4 v = *(const float4*)(po + (int64_t)(base + j) * 128);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
     }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
     const float f = 1.0f / den;
     *(uint2*)(out + row * 128 + lane * 4) =
         make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
@@ -623,6 +634,8 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
         sp = max(ceil_div(pages, per), 256 / PS);
     }
     sp = max(1, min(sp, pages));
+    // page-32 partitions hold whole 64-key tiles for the tensor-memory kernel
+    if (PS == 32 && split_tokens == 0 && (sp & 1) && sp < pages) ++sp;
     p->split_pages = sp;
     p->num_splits = ceil_div(pages, sp);
     p->split_tokens = sp * PS;
@@ -745,7 +758,12 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     P.max_seq_len = max_seq_len;
 
     cudaStream_t s = (cudaStream_t)stream;
-    if (page_size == 32)
+    // 49..128 query rows per KV head on E4M3 pages: tcgen05 kernel (one 128-row
+    // MMA tile); otherwise the mma.sync kernel
+    const bool use_tc = fp8 && P.R > 48 && P.R <= 128 && (page_size == 64 || !(plan.split_pages & 1));
+    if (use_tc)
+        rc = launch_verify_tc(tk, tv, P, s);
+    else if (page_size == 32)
         rc = fp8 ? launch<32, true>(tk, tv, P, s) : launch<32, false>(tk, tv, P, s);
     else
         rc = fp8 ? launch<64, true>(tk, tv, P, s) : launch<64, false>(tk, tv, P, s);
@@ -759,11 +777,18 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
         if (rc) return rc;
     }
     char buf[256];
-    snprintf(buf, sizeof buf,
-             "paged_attention_mma<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "
-             "split_tokens=%d grid=%dx%dx%d threads=%d reduce=%d",
-             page_size, fp8 ? "e4m3" : "bf16", P.R, P.NT, P.KW, P.SG, plan.num_splits, plan.split_tokens,
-             plan.num_splits, Hkv, B, (P.NT * P.KW + 1) * 32, plan.num_splits > 1 ? 1 : 0);
+    if (use_tc)
+        snprintf(buf, sizeof buf,
+                 "verify_tc<ps=%d,e4m3> rows=%d tile=128x64 splits=%d split_tokens=%d grid=%dx%dx%d threads=256 "
+                 "reduce=%d",
+                 page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B,
+                 plan.num_splits > 1 ? 1 : 0);
+    else
+        snprintf(buf, sizeof buf,
+                 "paged_attention_mma<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "
+                 "split_tokens=%d grid=%dx%dx%d threads=%d reduce=%d",
+                 page_size, fp8 ? "e4m3" : "bf16", P.R, P.NT, P.KW, P.SG, plan.num_splits, plan.split_tokens,
+                 plan.num_splits, Hkv, B, (P.NT * P.KW + 1) * 32, plan.num_splits > 1 ? 1 : 0);
     set_dispatch(buf);
     return FP8KV_OK;
 }
