@@ -55,7 +55,7 @@ SMALL = [
 
 
 @pytest.mark.parametrize("seq_lens,M,ps,window,Hq,Hkv", SMALL)
-@pytest.mark.parametrize("split_tokens", [0, 64])
+@pytest.mark.parametrize("split_tokens", [0, 64, 128])
 def test_attention_small_shapes(seq_lens, M, ps, window, Hq, Hkv, split_tokens):
     case = gen.layer_case(8000 + sum(seq_lens) + M, seq_lens, M, ps, window=window, Hq=Hq, Hkv=Hkv)
     run_case(case, split_tokens=split_tokens)
@@ -128,26 +128,27 @@ def test_attention_bad_seq_len_flagged():
 
 
 def test_verifier_rows_run_on_the_tensor_memory_kernel():
-    """108 rows per KV head (M=12, G=9) on an E4M3 cache dispatch to the
-    tcgen05 kernel; odd page-32 partitions and BF16 caches do not."""
+    """Up to 128 rows per KV head on an E4M3 cache with partitions of whole
+    128-key tiles dispatch to the tcgen05 kernel; other partitions to mma.sync."""
     case = gen.layer_case(8800, [777, 90], 12, 32, window=200)
     kc, vc, ks, vs = gpu_caches(case)
     okc, ovc = oracle_caches(case)
     ref = oracle_attention(case, okc, ovc)
-    for st, kernel in ((0, "verify_tc"), (64, "verify_tc"), (128, "verify_tc"), (96, "paged_attention_mma")):
+    for st, kernel in ((0, "attention_tc"), (128, "attention_tc"), (256, "attention_tc"),
+                       (64, "paged_attention_mma"), (96, "paged_attention_mma")):
         out = gpu_attention(case, kc, vc, ks, vs, split_tokens=st)
         assert fp8kv().fp8kv_last_dispatch().startswith(kernel), (st, fp8kv().fp8kv_last_dispatch())
         assert_close(out, ref, f"split={st}")
 
 
-@pytest.mark.parametrize("M,G", [(6, 9), (8, 16), (12, 10), (16, 8)])
+@pytest.mark.parametrize("M,G", [(1, 9), (2, 16), (6, 9), (8, 16), (12, 10), (16, 8), (3, 11)])
 def test_tensor_memory_kernel_row_counts(M, G):
-    """Row counts 54..128 through the tcgen05 kernel, both page sizes."""
+    """Row counts 9..128 through the tcgen05 kernel, both page sizes."""
     for ps in (32, 64):
         case = gen.layer_case(8900 + M + G + ps, [300, 1100], M, ps, Hq=2 * G, Hkv=2)
         kc, vc, ks, vs = gpu_caches(case)
         out = gpu_attention(case, kc, vc, ks, vs, split_tokens=256)
-        assert fp8kv().fp8kv_last_dispatch().startswith("verify_tc")
+        assert fp8kv().fp8kv_last_dispatch().startswith("attention_tc")
         okc, ovc = oracle_caches(case)
         assert_close(out, oracle_attention(case, okc, ovc), f"M={M} G={G} ps={ps}")
 

@@ -37,15 +37,23 @@ namespace fp8kv {
 int status_attention(unsigned int* s, int clear) { return read_status(s, clear); }
 
 constexpr int kMaxRowTiles = 9;          // M*G <= 144
-constexpr int kStageBudget = 96 * 1024;  // bytes of K/V stages per CTA
+// Bytes of K/V stages per CTA and key groups of the decode shape (one row
+// tile); overridable at build time for tuning sweeps.
+#ifndef FP8KV_STAGE_KB
+#define FP8KV_STAGE_KB 96
+#endif
+#ifndef FP8KV_DECODE_KEY_GROUPS
+#define FP8KV_DECODE_KEY_GROUPS 4
+#endif
+constexpr int kStageBudget = FP8KV_STAGE_KB * 1024;
 
 template <int PS, bool FP8>
 struct Cfg {
     static constexpr int kElem = FP8 ? 1 : 2;
     static constexpr int kTileBytes = PS * 128 * kElem;          // one (page, head) tile
     static constexpr int kStageBytes = 2 * kTileBytes;           // K + V
-    static constexpr int kStages = kStageBudget / kStageBytes;   // 12 / 6 / 6 / 3
-    static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int kStages = kStageBudget / kStageBytes;   // at 96 KiB: 12 / 6 / 6 / 3
+    static int smem_bytes(int stages) { return stages * kStageBytes + 1024 /*align*/ + 512 /*barriers*/; }
 };
 
 // Visible key range of query row r (M*G rows per KV head, row = m*G + g).
@@ -68,7 +76,7 @@ template <int PS, bool FP8>
 __global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
     using C = Cfg<PS, FP8>;
-    constexpr int S = C::kStages;
+    const int S = P.KW * P.SG;                                  // stages in use
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint64_t* bars = (uint64_t*)(smem + S * C::kStageBytes);   // full[S], empty[S]
@@ -558,6 +566,7 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <set>
 #include <utility>
 
@@ -634,8 +643,11 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
         sp = max(ceil_div(pages, per), 256 / PS);
     }
     sp = max(1, min(sp, pages));
-    // page-32 partitions hold whole 64-key tiles for the tensor-memory kernel
-    if (PS == 32 && split_tokens == 0 && (sp & 1) && sp < pages) ++sp;
+    // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
+    if (split_tokens == 0) {
+        const int tile_pages = tc_tile_tokens() / PS;
+        sp = (sp + tile_pages - 1) / tile_pages * tile_pages;
+    }
     p->split_pages = sp;
     p->num_splits = ceil_div(pages, sp);
     p->split_tokens = sp * PS;
@@ -651,14 +663,15 @@ static size_t ws_bytes(int B, int M, int Hq, const Plan& p) {
 // made under CUDA-graph capture issue no attribute change).
 static int ensure_smem(const void* kern, int bytes) {
     static std::mutex mu;
-    static std::set<std::pair<int, const void*>> done;
+    static std::map<std::pair<int, const void*>, int> done;   // largest size opted in so far
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return FP8KV_ERR_CUDA;
     std::lock_guard<std::mutex> lock(mu);
-    if (done.count({dev, kern})) return FP8KV_OK;
+    auto it = done.find({dev, kern});
+    if (it != done.end() && it->second >= bytes) return FP8KV_OK;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return FP8KV_ERR_CUDA;
-    done.insert({dev, kern});
+    done[{dev, kern}] = bytes;
     return FP8KV_OK;
 }
 
@@ -666,9 +679,9 @@ template <int PS, bool FP8>
 static int launch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
     using C = Cfg<PS, FP8>;
     auto kern = paged_attention_kernel<PS, FP8>;
-    if (ensure_smem((const void*)kern, C::kSmem)) return FP8KV_ERR_CUDA;
+    if (ensure_smem((const void*)kern, C::smem_bytes(std::max(C::kStages, P.KW * P.SG)))) return FP8KV_ERR_CUDA;
     dim3 grid(P.num_splits, P.Hkv, P.B);
-    kern<<<grid, (P.NT * P.KW + 1) * 32, C::kSmem, s>>>(tk, tv, P);
+    kern<<<grid, (P.NT * P.KW + 1) * 32, C::smem_bytes(P.KW * P.SG), s>>>(tk, tv, P);
     return launch_status();
 }
 
@@ -746,10 +759,15 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
         // idle; each group keeps at least two stages in flight when it can
         const int stages = page_size == 32 ? (fp8 ? Cfg<32, true>::kStages : Cfg<32, false>::kStages)
                                            : (fp8 ? Cfg<64, true>::kStages : Cfg<64, false>::kStages);
-        int kw = P.NT == 1 ? 4 : (P.NT == 2 ? 2 : 1);
-        kw = std::max(1, std::min(kw, stages / 2));
+        int kw = P.NT == 1 ? FP8KV_DECODE_KEY_GROUPS : (P.NT == 2 ? 2 : 1);
+        kw = std::max(1, std::min(kw, stages));
+        int sg = std::max(1, stages / kw);
+        // the epilogue merges the key groups' rows through the stage ring
+        const int elem = fp8 ? 1 : 2, stage_bytes = 2 * page_size * 128 * elem;
+        const int merge = kw * P.NT * 16 * 132 * 4;
+        while (kw * sg * stage_bytes < merge) ++sg;
         P.KW = kw;
-        P.SG = stages / kw;
+        P.SG = sg;
     }
     P.window_left = window_left;
     P.split_pages = plan.split_pages;
@@ -758,9 +776,9 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     P.max_seq_len = max_seq_len;
 
     cudaStream_t s = (cudaStream_t)stream;
-    // 49..128 query rows per KV head on E4M3 pages: tcgen05 kernel (one 128-row
-    // MMA tile); otherwise the mma.sync kernel
-    const bool use_tc = fp8 && P.R > 48 && P.R <= 128 && (page_size == 64 || !(plan.split_pages & 1));
+    // up to 128 query rows per KV head on E4M3 pages, partitions of whole
+    // 128-key tiles: tcgen05 kernel (one 128-row MMA tile); otherwise mma.sync
+    const bool use_tc = fp8 && P.R <= 128 && (plan.split_tokens % tc_tile_tokens()) == 0;
     if (use_tc)
         rc = launch_verify_tc(tk, tv, P, s);
     else if (page_size == 32)
@@ -779,7 +797,7 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     char buf[256];
     if (use_tc)
         snprintf(buf, sizeof buf,
-                 "verify_tc<ps=%d,e4m3> rows=%d tile=128x64 splits=%d split_tokens=%d grid=%dx%dx%d threads=256 "
+                 "attention_tc<ps=%d,e4m3> rows=%d tile=128x128 splits=%d split_tokens=%d grid=%dx%dx%d threads=448 "
                  "reduce=%d",
                  page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B,
                  plan.num_splits > 1 ? 1 : 0);

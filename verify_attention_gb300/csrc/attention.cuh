@@ -24,5 +24,6 @@ struct AttnParams {
 // FP8KV_ERR_UNSUPPORTED when the shape is not one it implements.
 int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s);
 int status_attention_tc(unsigned int* s, int clear);
+int tc_tile_tokens();   // keys per tile of the tcgen05 kernel
 
 }  // namespace fp8kv

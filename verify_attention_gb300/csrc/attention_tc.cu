@@ -1,24 +1,32 @@
-// attention_tc.cu -- paged verifier attention on the 5th-generation tensor
-// cores (tcgen05), for M x G query rows per KV head in (48, 128]: the M = 12,
-// G = 9 verifier of "Laguna S 2.1 INT4 -- calibrated FP8 KV on Intel B70"
-// ("Contract": width 12; "Initial optimization order", item 2: exact M12 paged
-// attention) over the E4M3 cache ("Laguna S 2.1 KV-cache precision decision",
-// property table: scale/dequantize on read).
+// attention_tc.cu -- paged decode / verifier attention on the 5th-generation
+// tensor cores (tcgen05) for up to 128 query rows per KV head: M = 1 decode
+// (9 rows) and the M = 12 verifier (108 rows) of "Laguna S 2.1 INT4 --
+// calibrated FP8 KV on Intel B70" ("Contract"; "Initial optimization order",
+// item 2: exact q1/M12 paged attention) over the E4M3 cache ("Laguna S 2.1
+// KV-cache precision decision", property table: "scale/dequantize or use native
+// FP8 attention").
 //
-// One CTA per (partition, KV head, sequence), 8 warps:
-//   warp 0     TMA producer: 64-key tiles of E4M3 K and V (one page of 64 or
-//              two pages of 32) into a 4-deep staging ring; owns TMEM.
-//   warp 1     MMA issuer (one thread): S = Q.K^T (M=128, N=64, K=128) into a
-//              double-buffered TMEM tile, then O += P.V (M=128, N=128, K=64)
-//              into TMEM; completion through tcgen05.commit -> mbarrier.
-//   warps 2-3  converters: E4M3 -> f16 (exact) into 128B-swizzled smem tiles,
-//              K as the K-major B operand, V as the MN-major B operand.
-//   warps 4-7  softmax, one thread per query row: tcgen05.ld of the S row,
-//              mask, online softmax (log2 domain, lazy O rescale when the row
-//              maximum grows by more than 2^8), P as f16 written back over S
-//              with tcgen05.st; it becomes the A operand of P.V straight from
-//              TMEM.  Q lives in TMEM too (A operand of Q.K^T).
-// TMEM: Q 64 columns, S/P 2 x 64, O 128 (512 allocated).
+// Q.K^T runs natively in FP8: the E4M3 K tile is the B operand straight from
+// the TMA staging buffer (its 128-byte rows with the 128-byte swizzle are the
+// K-major operand layout), and each Q row is split into two E4M3 terms after a
+// per-row power-of-two scale, q' = q * 2^sh = Q_hi + Q_lo, which is exact for
+// every bf16 element within 2^-10 of the row maximum (the rest is off by at
+// most 2^-17 of the row maximum); two accumulating MMAs give S = q'.K.  P.V
+// runs in f16: P (softmax weights) is written to tensor memory and is the A
+// operand, V is widened E4M3 -> f16 (exact) into a swizzled MN-major tile.
+//
+// One CTA per (partition, KV head, sequence), 16 warps:
+//   warp 0          TMA producer (128-key tiles: K and V E4M3, 2 or 4 pages);
+//                   allocates and frees the tensor memory
+//   warp 1          MMA issuer (one thread); completion via tcgen05.commit
+//   warps 2,3,12-15 V converters (192 threads)
+//   warps 4-11      softmax: warps 4+q and 8+q share TMEM lane quarter q (32
+//                   query rows, one per thread) and split the tile's 128 key
+//                   columns in halves; the row maximum of a tile is exchanged
+//                   through shared memory.  Masks, online softmax in the log2
+//                   domain, lazy O rescale (only when a row maximum grows by
+//                   more than 2^8), P to TMEM.
+// TMEM columns: Q_hi 0-31, Q_lo 32-63, S/P 2 x 128 (64-319), O 320-447.
 #include <mutex>
 #include <set>
 #include <utility>
@@ -33,28 +41,36 @@ int status_attention_tc(unsigned int* s, int clear) { return read_status(s, clea
 
 namespace tc {
 
-constexpr int NK = 64;                          // keys per tile
-constexpr int STAGES = 4;                       // E4M3 staging tiles
-constexpr int STG_BYTES = 2 * NK * 128;         // K + V E4M3: 16 KiB
-constexpr int F16_BYTES = 2 * NK * 256;         // K + V f16: 32 KiB
-constexpr int SMEM = STAGES * STG_BYTES + 2 * F16_BYTES + 1024 + 512;
-constexpr uint32_t TM_Q = 0, TM_S = 64, TM_O = 256, TM_COLS = 512;
-constexpr int THREADS = 256;
+constexpr int NK = 128;                         // keys per tile
+constexpr int STAGES = 3;                       // E4M3 staging tiles (K + V)
+constexpr int STG_K = NK * 128;                 // 16 KiB
+constexpr int STG_BYTES = 2 * STG_K;            // 32 KiB
+constexpr int VBUFS = 3;                        // f16 V tiles
+constexpr int VBUF_BYTES = NK * 256;            // 32 KiB
+constexpr int XCH_BYTES = 3 * 2 * 128 * 4;      // [tile parity 0, parity 1, row sums][half][row]
+constexpr int SMEM = STAGES * STG_BYTES + VBUFS * VBUF_BYTES + XCH_BYTES + 1024 + 512;
+constexpr uint32_t TM_QH = 0, TM_QL = 32, TM_S = 64, TM_O = 320, TM_COLS = 512;
+constexpr int WARPS = 16, THREADS = WARPS * 32;
+constexpr int CONV_WARPS = 6, CONV_THREADS = CONV_WARPS * 32;
 
-// barrier slots
 enum {
     B_STG_FULL = 0,
     B_STG_EMPTY = B_STG_FULL + STAGES,
-    B_KV_FULL = B_STG_EMPTY + STAGES,
-    B_KV_EMPTY = B_KV_FULL + 2,
-    B_S_FULL = B_KV_EMPTY + 2,
+    B_V_FULL = B_STG_EMPTY + STAGES,
+    B_V_EMPTY = B_V_FULL + VBUFS,
+    B_S_FULL = B_V_EMPTY + VBUFS,
     B_P_FULL = B_S_FULL + 2,
     B_O_DONE = B_P_FULL + 2,
     B_O_FINAL = B_O_DONE + 1,
     B_Q_READY = B_O_FINAL + 1,
     B_MMA_IDLE = B_Q_READY + 1,
-    B_COUNT = B_MMA_IDLE + 1
+    B_PAIR = B_MMA_IDLE + 1,                    // one per TMEM lane quarter: the two softmax warps
+    B_COUNT = B_PAIR + 4
 };
+
+__device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
+__device__ __forceinline__ int converter_index(int warp) { return warp < 4 ? warp - 2 : warp - 10; }
+
 
 // Shared-memory matrix descriptor, 128-byte swizzle (layout type 2), sm_100
 // descriptor version 1; offsets in bytes.
@@ -63,17 +79,25 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B f16, A K-major.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+// Instruction descriptor: D fp32; A, B format code 0 (f16 for kind::f16,
+// E4M3 for kind::f8f6f4); A K-major; B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
     return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accum) {
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
     asm volatile(
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accum)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+        "r"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p; }" ::"r"(d),
+        "r"(a), "l"(b), "r"(id), "r"(acc)
         : "memory");
 }
 
@@ -88,55 +112,23 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 16 E4M3 codes (one 16-byte chunk) -> 16 f16 (two 16-byte chunks), exact.
-__device__ __forceinline__ void widen_chunk(uint4 c, uint4& lo, uint4& hi) {
-    lo.x = e4m3x2_to_f16x2(c.x);
-    lo.y = e4m3x2_to_f16x2(c.x >> 16);
-    lo.z = e4m3x2_to_f16x2(c.y);
-    lo.w = e4m3x2_to_f16x2(c.y >> 16);
-    hi.x = e4m3x2_to_f16x2(c.z);
-    hi.y = e4m3x2_to_f16x2(c.z >> 16);
-    hi.z = e4m3x2_to_f16x2(c.w);
-    hi.w = e4m3x2_to_f16x2(c.w >> 16);
-}
-
-// Converts one staged E4M3 tile (64 rows x 128 B, 128B-swizzled) into the f16
-// layout the MMA reads: two 64-column blocks (dims 0-63, 64-127) of 64 rows x
-// 128 B, 128B-swizzled.  The same layout serves as the K-major K operand and
-// the MN-major V operand.  Rows flagged in `zero_mask` (bit r) are written as
-// zeros.  64 threads, 8 chunks each; the write order alternates so that each
-// quarter-warp hits 8 distinct 16-byte bank groups.
-__device__ __forceinline__ void convert_tile(const uint8_t* src, uint8_t* dst, int ct, uint64_t zero_mask) {
-#pragma unroll 2
-    for (int u = 0; u < 8; ++u) {
-        const int i = ct + 64 * u;
-        const int r = i >> 3, c = i & 7;
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-        if (!((zero_mask >> r) & 1)) {
-            const uint4 code = *(const uint4*)(src + r * 128 + (((c ^ r) & 7) << 4));
-            widen_chunk(code, lo, hi);
-        }
-        uint8_t* blk = dst + (c >> 2) * (NK * 128) + r * 128;
-        const int c16 = 2 * (c & 3);
-        if (c < 4) {
-            *(uint4*)(blk + (((c16 ^ r) & 7) << 4)) = lo;
-            *(uint4*)(blk + ((((c16 + 1) ^ r) & 7) << 4)) = hi;
-        } else {
-            *(uint4*)(blk + ((((c16 + 1) ^ r) & 7) << 4)) = hi;
-            *(uint4*)(blk + (((c16 ^ r) & 7) << 4)) = lo;
-        }
-    }
+__device__ __forceinline__ uint32_t e4m3x2_to_f32x2_lo(uint32_t codes, float& a, float& b) {
+    const uint32_t h = e4m3x2_to_f16x2(codes);
+    a = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+    b = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+    return h;
 }
 
 template <int PS>
-__global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                              const __grid_constant__ CUtensorMap tm_v,
-                                                              AttnParams P) {
+__global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                 const __grid_constant__ CUtensorMap tm_v,
+                                                                 AttnParams P) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* stg = smem;                                   // STAGES x 16 KiB
-    uint8_t* f16buf = smem + STAGES * STG_BYTES;           // 2 x 32 KiB
-    uint64_t* bars = (uint64_t*)(f16buf + 2 * F16_BYTES);
+    uint8_t* stg = smem;                                    // STAGES x (K 16 KiB, V 16 KiB)
+    uint8_t* vbuf = smem + STAGES * STG_BYTES;              // VBUFS x 32 KiB
+    float* xch = (float*)(vbuf + VBUFS * VBUF_BYTES);       // [parity][half][row]
+    uint64_t* bars = (uint64_t*)((uint8_t*)xch + XCH_BYTES);
     uint32_t* tmem_slot = (uint32_t*)(bars + B_COUNT);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -157,25 +149,28 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
     if (split >= nsplit_b) return;
     const int page_begin = first_page + split * P.split_pages;
     const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
-    constexpr int PPT = NK / PS;                          // pages per tile
+    constexpr int PPT = NK / PS;                            // pages per tile
     const int n_tiles = (n_pages + PPT - 1) / PPT;
     const int k_begin = page_begin * PS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(B_STG_FULL + s), 1);
-            mbar_init(bar(B_STG_EMPTY + s), 2);
+            mbar_init(bar(B_STG_EMPTY + s), 1 + CONV_WARPS);   // QK commit + converters
+        }
+        for (int s = 0; s < VBUFS; ++s) {
+            mbar_init(bar(B_V_FULL + s), CONV_WARPS);
+            mbar_init(bar(B_V_EMPTY + s), 1);
         }
         for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_KV_FULL + s), 2);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
             mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_P_FULL + s), 4);
+            mbar_init(bar(B_P_FULL + s), 8);
         }
         mbar_init(bar(B_O_DONE), 1);
         mbar_init(bar(B_O_FINAL), 1);
-        mbar_init(bar(B_Q_READY), 4);
+        mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
+        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -204,8 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
             const int cnt = min(32, n_pages - base);
             for (int j = 0; j < cnt; ++j) {
                 const int phys = __shfl_sync(0xffffffffu, mine, j);
-                const int i = base + j;                   // page index in the partition
-                const int t = i / PPT, pin = i % PPT;     // tile, page within the tile
+                const int i = base + j;
+                const int t = i / PPT, pin = i % PPT;
                 const int s = t % STAGES, use = t / STAGES;
                 if (lane == 0) {
                     if (pin == 0) {
@@ -215,9 +210,8 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
                     }
                     if (ok) {
                         const uint32_t dk = smem_u32(stg + s * STG_BYTES + pin * PS * 128);
-                        const uint32_t dv = dk + NK * 128;
                         tma_load_3d(dk, &tm_k, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
-                        tma_load_3d(dv, &tm_v, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
+                        tma_load_3d(dk + STG_K, &tm_v, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -233,37 +227,40 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc_f16(128, NK, false);
-            constexpr uint32_t ID_PV = idesc_f16(128, 128, true);
+            constexpr uint32_t ID_QK = idesc(128, NK, false);     // kind::f8f6f4, E4M3 x E4M3
+            constexpr uint32_t ID_PV = idesc(128, 128, true);     // kind::f16, V MN-major
             ok = mbar_wait(bar(B_Q_READY), 0);
             fence_after();
             for (int t = 0; t <= n_tiles && ok; ++t) {
                 if (t < n_tiles) {
-                    const int kb = t & 1;
-                    ok = mbar_wait(bar(B_KV_FULL + kb), (t >> 1) & 1);
+                    const int s = t % STAGES, sb = t & 1;
+                    ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);
                     if (!ok) break;
                     fence_after();
-                    const uint32_t kf = smem_u32(f16buf + kb * F16_BYTES);
+                    const uint32_t kt = smem_u32(stg + s * STG_BYTES);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t bd = sdesc(kf + (ks >> 2) * (NK * 128) + (ks & 3) * 32, 16, 1024);
-                        mma_ts(tmem + TM_S + kb * 64, tmem + TM_Q + 8 * ks, bd, ID_QK, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t bd = sdesc(kt + ks * 32, 16, 1024);
+                        mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QH + 8 * ks, bd, ID_QK, ks > 0);
+                        mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QL + 8 * ks, bd, ID_QK, 1);
                     }
-                    mma_commit(bar(B_S_FULL + kb));
+                    mma_commit(bar(B_S_FULL + sb));
+                    mma_commit(bar(B_STG_EMPTY + s));        // K of this stage read
                 }
                 if (t >= 1) {
-                    const int u = t - 1, ub = u & 1;
+                    const int u = t - 1, ub = u & 1, vb = u % VBUFS;
                     ok = mbar_wait(bar(B_P_FULL + ub), (u >> 1) & 1);
+                    if (ok) ok = mbar_wait(bar(B_V_FULL + vb), (u / VBUFS) & 1);
                     if (!ok) break;
                     fence_after();
-                    const uint32_t vf = smem_u32(f16buf + ub * F16_BYTES + NK * 256);
+                    const uint32_t vf = smem_u32(vbuf + vb * VBUF_BYTES);
 #pragma unroll
                     for (int kk = 0; kk < NK / 16; ++kk) {
                         const uint64_t bd = sdesc(vf + kk * 2048, NK * 128, 1024);
-                        mma_ts(tmem + TM_O, tmem + TM_S + ub * 64 + 8 * kk, bd, ID_PV, (u > 0 || kk > 0));
+                        mma_f16_ts(tmem + TM_O, tmem + TM_S + ub * 128 + 8 * kk, bd, ID_PV, (u > 0 || kk > 0));
                     }
                     mma_commit(bar(B_O_DONE));
-                    mma_commit(bar(B_KV_EMPTY + ub));
+                    mma_commit(bar(B_V_EMPTY + vb));
                     if (u == n_tiles - 1) mma_commit(bar(B_O_FINAL));
                 }
             }
@@ -272,39 +269,71 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
             mbar_wait(bar(B_MMA_IDLE), 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ---------------------------------------------------------- converters
-        const int ct = threadIdx.x - 64;
+    } else if (is_converter(warp)) {
+        // ---------------------------------------------------------- V widening
+        // 128 keys x 8 chunks of 16 E4M3 values -> two 64-dim blocks of
+        // 128 x 128 B f16 (128B-swizzled): the MN-major B operand of P.V.
+        // Keys outside every row's range are written as zeros, so stale or NaN
+        // bytes there cannot reach the output.
+        const int ct = converter_index(warp) * 32 + lane;
         for (int t = 0; t < n_tiles; ++t) {
-            const int s = t % STAGES, kb = t & 1;
+            const int s = t % STAGES, vb = t % VBUFS;
             ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);
-            if (ok && t >= 2) ok = mbar_wait(bar(B_KV_EMPTY + kb), ((t >> 1) - 1) & 1);
+            if (ok && t >= VBUFS) ok = mbar_wait(bar(B_V_EMPTY + vb), ((t / VBUFS) - 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            // rows of this tile outside every query row's range read as zeros
-            // in V (stale or NaN bytes must not reach P.V); K needs no care
-            // since those logits are masked
             const int k0 = k_begin + t * NK;
             const int pages_here = min(PPT, n_pages - t * PPT);
-            const int zlo = max(0, min(NK, lo0 - k0));                       // rows [0, zlo) before every window
-            const int zhi = max(0, min(min(NK, pages_here * PS), L - k0));   // rows [zhi, NK) past the end
-            const uint64_t below = zlo >= 64 ? ~0ull : ((1ull << zlo) - 1);
-            const uint64_t keep = zhi >= 64 ? ~0ull : ((1ull << zhi) - 1);
-            const uint64_t zmask = below | ~keep;
-            const uint8_t* src = stg + s * STG_BYTES;
-            uint8_t* dst = f16buf + kb * F16_BYTES;
-            convert_tile(src, dst, ct, 0);
-            convert_tile(src + NK * 128, dst + NK * 256, ct, zmask);
+            const int zlo = max(0, min(NK, lo0 - k0));
+            const int zhi = max(0, min(min(NK, pages_here * PS), L - k0));
+            const uint8_t* src = stg + s * STG_BYTES + STG_K;
+            uint8_t* dst = vbuf + vb * VBUF_BYTES;
+            constexpr int PER = (NK * 8 + CONV_THREADS - 1) / CONV_THREADS;   // chunks per thread
+            uint4 code[PER];
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int i = ct + CONV_THREADS * u;
+                const int r = i >> 3, c = i & 7;
+                code[u] = (i < NK * 8 && r >= zlo && r < zhi)
+                              ? *(const uint4*)(src + r * 128 + (((c ^ r) & 7) << 4))
+                              : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int i = ct + CONV_THREADS * u;
+                if (i >= NK * 8) break;
+                const int r = i >> 3, c = i & 7;
+                uint4 lo, hi;
+                lo.x = e4m3x2_to_f16x2(code[u].x);
+                lo.y = e4m3x2_to_f16x2(code[u].x >> 16);
+                lo.z = e4m3x2_to_f16x2(code[u].y);
+                lo.w = e4m3x2_to_f16x2(code[u].y >> 16);
+                hi.x = e4m3x2_to_f16x2(code[u].z);
+                hi.y = e4m3x2_to_f16x2(code[u].z >> 16);
+                hi.z = e4m3x2_to_f16x2(code[u].w);
+                hi.w = e4m3x2_to_f16x2(code[u].w >> 16);
+                uint8_t* blk = dst + (c >> 2) * (NK * 128) + r * 128;
+                const int c16 = 2 * (c & 3);
+                // alternate the order so each quarter-warp covers all 32 banks
+                if (c < 4) {
+                    *(uint4*)(blk + (((c16 ^ r) & 7) << 4)) = lo;
+                    *(uint4*)(blk + ((((c16 + 1) ^ r) & 7) << 4)) = hi;
+                } else {
+                    *(uint4*)(blk + ((((c16 + 1) ^ r) & 7) << 4)) = hi;
+                    *(uint4*)(blk + (((c16 ^ r) & 7) << 4)) = lo;
+                }
+            }
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(bar(B_STG_EMPTY + s));
-                mbar_arrive(bar(B_KV_FULL + kb));
+                mbar_arrive(bar(B_V_FULL + vb));
             }
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int wq = warp & 3;
+        const int wq = warp & 3, half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
+        const bool active = wq * 32 < P.R;                  // quarter holds at least one real row
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
         const int rr = min(r, P.R - 1);
         const int m = rr / P.G;
@@ -312,35 +341,54 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
         float mult;
         {
-            // Q row -> f16 with a power-of-two prescale putting the row maximum
-            // in [2^14, 2^15) (exact for bf16 inputs), folded into the logit
-            // multiplier with k_scale * sm_scale * log2(e)
-            uint32_t qw[64];
+            // q' = q * 2^sh with the row maximum in [128, 256); half 0 stores
+            // Q_hi = e4m3(q'), half 1 stores Q_lo = e4m3(q' - Q_hi)
             float amax = 0.f;
             const uint4* src = (const uint4*)(P.q + (((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G) * 128);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const uint4 w = (r < P.R) ? src[u] : make_uint4(0, 0, 0, 0);
-                qw[4 * u] = w.x;
-                qw[4 * u + 1] = w.y;
-                qw[4 * u + 2] = w.z;
-                qw[4 * u + 3] = w.w;
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
                                          fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
                 amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
                                          fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
             }
-            int e = 14;
+            int e = 7;
             const uint32_t ab = __float_as_uint(amax);
             if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
                 const int be = (int)((ab >> 23) & 0xff);
                 e = be ? be - 127 : -127;
             }
-            const int sh = max(-100, min(100, 14 - e));
+            const int sh = max(-100, min(100, 7 - e));
             const float scale = ldexpf(1.0f, sh);
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {   // 64 dims per pass: 16 TMEM columns
+                uint32_t qw[32], outw[16];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) qw[j] = pack_f16x2(bf16_lo(qw[j]) * scale, bf16_hi(qw[j]) * scale);
-            tmem_st_x64(lane_base + TM_Q, qw);
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 w = (r < P.R) ? src[8 * hh + u] : make_uint4(0, 0, 0, 0);
+                    qw[4 * u] = w.x;
+                    qw[4 * u + 1] = w.y;
+                    qw[4 * u + 2] = w.z;
+                    qw[4 * u + 3] = w.w;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t w0 = qw[2 * j], w1 = qw[2 * j + 1];
+                    const float a0 = bf16_lo(w0) * scale, a1 = bf16_hi(w0) * scale;
+                    const float a2 = bf16_lo(w1) * scale, a3 = bf16_hi(w1) * scale;
+                    const uint32_t h01 = e4m3x2(a0, a1), h23 = e4m3x2(a2, a3);
+                    if (half == 0) {
+                        outw[j] = h01 | (h23 << 16);
+                    } else {
+                        float d0, d1, d2, d3;
+                        e4m3x2_to_f32x2_lo(h01, d0, d1);
+                        e4m3x2_to_f32x2_lo(h23, d2, d3);
+                        outw[j] = e4m3x2(a0 - d0, a1 - d1) | (e4m3x2(a2 - d2, a3 - d3) << 16);
+                    }
+                }
+                tmem_st_x16(lane_base + (half == 0 ? TM_QH : TM_QL) + 16 * hh, outw);
+            }
             tmem_wait_st();
             mult = (*P.k_scale) * P.sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
         }
@@ -348,70 +396,85 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY));
 
-        // warp-uniform bounds: tiles strictly inside every row's range skip masking
         int pmin = p_r, lomax = lo_r;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, off));
             lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, off));
         }
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;               // l_run: this half's columns only
         for (int t = 0; t < n_tiles; ++t) {
             const int sb = t & 1;
             ok = mbar_wait(bar(B_S_FULL + sb), (t >> 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             fence_after();
-            uint32_t sv[64];
-            tmem_ld_x64(lane_base + TM_S + sb * 64, sv);
-            tmem_wait_ld();
-            const int k0 = k_begin + t * NK;
-            const bool need_mask = (k0 + NK - 1 > pmin) || (k0 < lomax);
-            float smax = -INFINITY;
+            if (active) {
+                const uint32_t scol = lane_base + TM_S + sb * 128 + 64 * half;
+                const int k0 = k_begin + t * NK + 64 * half;   // first key of this half
+                uint32_t sv[64];
+                tmem_ld_x64(scol, sv);
+                tmem_wait_ld();
+                if ((k0 + 63 > pmin) || (k0 < lomax)) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                float x = __uint_as_float(sv[j]);
-                if (need_mask && (k0 + j > p_r || k0 + j < lo_r)) x = -INFINITY;
-                sv[j] = __float_as_uint(x);
-                smax = fmaxf(smax, x);
-            }
-            const float tmax = smax * mult;
-            const bool rescale = (m_run != -INFINITY) && (tmax > m_run + 8.0f);
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O rows of this warp hold P.V up to tile t-1: wait for it, then scale
-                const bool okw = mbar_wait(bar(B_O_DONE), (t - 1) & 1);
-                if (!__all_sync(0xffffffffu, okw)) { ok = false; break; }
-                fence_after();
-                const float alpha = rescale ? ex2(m_run - tmax) : 1.0f;
+                    for (int j = 0; j < 64; ++j)
+                        if (k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
+                }
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) {
+                    m4[0] = fmaxf(m4[0], __uint_as_float(sv[j]));
+                    m4[1] = fmaxf(m4[1], __uint_as_float(sv[j + 1]));
+                    m4[2] = fmaxf(m4[2], __uint_as_float(sv[j + 2]));
+                    m4[3] = fmaxf(m4[3], __uint_as_float(sv[j + 3]));
+                }
+                xch[(sb * 2 + half) * 128 + r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                // exchange with the partner warp (bounded wait, phase t of the pair barrier)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_PAIR + wq));
+                ok = mbar_wait(bar(B_PAIR + wq), t & 1);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                const float smax = fmaxf(xch[sb * 256 + r], xch[sb * 256 + 128 + r]);
+                const float tmax = smax * mult;
+                const bool rescale = (m_run != -INFINITY) && (tmax > m_run + 8.0f);
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O holds P.V up to tile t-1: wait for it, then rescale this half
+                    const bool okw = mbar_wait(bar(B_O_DONE), (t - 1) & 1);
+                    if (!__all_sync(0xffffffffu, okw)) { ok = false; break; }
+                    fence_after();
+                    const float alpha = rescale ? ex2(m_run - tmax) : 1.0f;
 #pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t ov[32];
-                    tmem_ld_x32(lane_base + TM_O + c, ov);
-                    tmem_wait_ld();
+                    for (int c = 0; c < 64; c += 32) {
+                        uint32_t ov[32];
+                        tmem_ld_x32(lane_base + TM_O + 64 * half + c, ov);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-                    tmem_st_x32(lane_base + TM_O + c, ov);
+                        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+                        tmem_st_x32(lane_base + TM_O + 64 * half + c, ov);
+                    }
+                    tmem_wait_st();
+                    if (rescale) {
+                        l_run *= alpha;
+                        m_run = tmax;
+                    }
                 }
+                if (m_run == -INFINITY) m_run = tmax;
+                const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
+                // P = 2^(s*mult - m) as f16 (masked keys are -inf and give 0);
+                // both halves' S reads are complete (pair barrier above)
+                float sum0 = 0.f, sum1 = 0.f;
+                uint32_t pw[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * j]), mult, neg));
+                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * j + 1]), mult, neg));
+                    sum0 += p0;
+                    sum1 += p1;
+                    pw[j] = pack_f16x2(p0, p1);
+                }
+                tmem_st_x32(lane_base + TM_S + sb * 128 + 32 * half, pw);
+                l_run += sum0 + sum1;
                 tmem_wait_st();
-                if (rescale) {
-                    l_run *= alpha;
-                    m_run = tmax;
-                }
             }
-            if (m_run == -INFINITY) m_run = tmax;           // first visible keys of this row
-            float sum = 0.f;
-            uint32_t pw[32];
-            const float neg = (m_run == -INFINITY) ? 0.f : -m_run;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float x0 = __uint_as_float(sv[2 * j]), x1 = __uint_as_float(sv[2 * j + 1]);
-                const float p0 = (x0 == -INFINITY) ? 0.f : ex2(fmaf(x0, mult, neg));
-                const float p1 = (x1 == -INFINITY) ? 0.f : ex2(fmaf(x1, mult, neg));
-                sum += p0 + p1;
-                pw[j] = pack_f16x2(p0, p1);
-            }
-            l_run += sum;
-            tmem_st_x32(lane_base + TM_S + sb * 64, pw);
-            tmem_wait_st();
             fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_P_FULL + sb));
@@ -419,20 +482,29 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
         // ------------------------------------------------------------ epilogue
         if (ok) ok = mbar_wait(bar(B_O_FINAL), 0);
         ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
+        if (ok && active) {
             fence_after();
+            // row sums of both halves: phase n_tiles of the pair barrier
+            xch[(4 + half) * 128 + r] = l_run;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_PAIR + wq));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PAIR + wq), n_tiles & 1));
+        }
+        if (ok && active) {
+            const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const float vs = *P.v_scale;
             const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
             const bool direct = nsplit_b == 1;
-            const float f = direct ? vs / l_run : vs;
+            const float f = direct ? vs / l_tot : vs;
 #pragma unroll 1
-            for (int c = 0; c < 128; c += 32) {
+            for (int c = 0; c < 64; c += 32) {
                 uint32_t ov[32];
-                tmem_ld_x32(lane_base + TM_O + c, ov);
+                tmem_ld_x32(lane_base + TM_O + 64 * half + c, ov);
                 tmem_wait_ld();
                 if (r < P.R) {
+                    const int d0 = 64 * half + c;
                     if (direct) {
-                        uint4* dst = (uint4*)(P.out + row_idx * 128 + c);
+                        uint4* dst = (uint4*)(P.out + row_idx * 128 + d0);
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4)
                             dst[v4] = make_uint4(
@@ -441,7 +513,7 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
                                 pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                                 pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
                     } else {
-                        float4* dst = (float4*)(P.ws_o + (row_idx * P.num_splits + split) * 128 + c);
+                        float4* dst = (float4*)(P.ws_o + (row_idx * P.num_splits + split) * 128 + d0);
 #pragma unroll
                         for (int v4 = 0; v4 < 8; ++v4)
                             dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * f, __uint_as_float(ov[4 * v4 + 1]) * f,
@@ -450,9 +522,9 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
                     }
                 }
             }
-            if (r < P.R && !direct) {
+            if (r < P.R && !direct && half == 0) {
                 P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
-                P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_run;
+                P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_tot;
             }
         }
     }
@@ -468,12 +540,15 @@ __global__ void __launch_bounds__(THREADS, 1) verify_tc_kernel(const __grid_cons
 
 }  // namespace tc
 
+int tc_tile_tokens() { return tc::NK; }
+
 int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
-    if (P.R > 128 || P.R <= 48) return FP8KV_ERR_UNSUPPORTED;
-    if (P.page_size == 32 && (P.split_pages & 1)) return FP8KV_ERR_UNSUPPORTED;
+    if (P.R > 128) return FP8KV_ERR_UNSUPPORTED;
+    if ((P.split_pages * P.page_size) % tc::NK) return FP8KV_ERR_UNSUPPORTED;
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
-    const void* kern = P.page_size == 32 ? (const void*)tc::verify_tc_kernel<32> : (const void*)tc::verify_tc_kernel<64>;
+    const void* kern = P.page_size == 32 ? (const void*)tc::attention_tc_kernel<32>
+                                         : (const void*)tc::attention_tc_kernel<64>;
     {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return FP8KV_ERR_CUDA;
@@ -486,9 +561,9 @@ int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnPar
     }
     dim3 grid(P.num_splits, P.Hkv, P.B);
     if (P.page_size == 32)
-        tc::verify_tc_kernel<32><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
+        tc::attention_tc_kernel<32><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
     else
-        tc::verify_tc_kernel<64><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
+        tc::attention_tc_kernel<64><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
     return launch_status();
 }
 

@@ -129,10 +129,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
     if (ok) return true;
     const uint64_t start = globaltimer();
     while (true) {
+        // suspends until the phase completes or 0.5 ms pass: no hot spinning
         asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
             : "=r"(ok)
-            : "r"(bar), "r"(phase)
+            : "r"(bar), "r"(phase), "r"(500000u)
             : "memory");
         if (ok) return true;
         if (globaltimer() - start > 2000000000ull) {
