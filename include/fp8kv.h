@@ -140,8 +140,12 @@ int fp8kv_paged_attention_plan(int B, int M, int Hq, int Hkv, int D, int page_si
                                int max_seq_len, int window_left, int split_tokens,
                                int* num_splits, int* split_tokens_out);
 
-/* Workspace bytes fp8kv_paged_attention needs for the same arguments
- * (0 when one partition per sequence suffices; (size_t)-1 on bad arguments). */
+/* Workspace bytes fp8kv_paged_attention needs for the same arguments: the
+ * split-KV partials when a sequence spans several partitions, plus, for 17 to
+ * 128 query rows per KV head, an E4M3 split of Q (two 128-byte rows and a
+ * multiplier per query row) read by the tensor-memory kernel.  The size does
+ * not depend on the cache dtype.  0 when neither applies; (size_t)-1 on bad
+ * arguments. */
 size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D,
                                             int page_size, int max_seq_len, int window_left,
                                             int split_tokens);

@@ -84,6 +84,8 @@ __global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_ke
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_cons = P.NT * P.KW;
+    pdl_launch_dependents();
+    pdl_wait();
     const int L = P.seq_lens[b];
     if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
         if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
@@ -501,6 +503,8 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
                                                           int Hq, int mpps, int page_size, int window_left,
                                                           int split_pages, int num_splits, int max_seq_len,
                                                           uint16_t* out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= (int64_t)B * M * Hq) return;
@@ -635,12 +639,13 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
     if (split_tokens > 0) {
         sp = split_tokens / PS;
     } else {
-        // about four waves of two CTAs per SM over all (sequence, head)
-        // units, with at least 256 keys per partition
+        // about two partitions per SM over all (sequence, head) units, with
+        // at least 1024 keys per partition: per-CTA set-up and the partial
+        // write-back make short partitions expensive
         const int64_t units = (int64_t)max(B, 1) * Hkv;
-        const int64_t target = 8LL * num_sms();
+        const int64_t target = 2LL * num_sms();
         const int per = (int)std::max<int64_t>(1, (target + units - 1) / units);
-        sp = max(ceil_div(pages, per), 256 / PS);
+        sp = max(ceil_div(pages, per), 1024 / PS);
     }
     sp = max(1, min(sp, pages));
     // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
@@ -654,9 +659,23 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
     return FP8KV_OK;
 }
 
-static size_t ws_bytes(int B, int M, int Hq, const Plan& p) {
-    if (p.num_splits <= 1) return 0;
-    return (size_t)B * M * Hq * p.num_splits * (128 + 2) * sizeof(float);
+// Workspace: [Q split for the tcgen05 kernel][partial O][partial (m, l)].
+// The Q split (E4M3 hi and lo rows and a per-row logit multiplier) is
+// reserved for every shape the tcgen05 kernel may take (16 < M*G <= 128).
+static bool tc_rows(int M, int Hq, int Hkv) {
+    const int R = M * (Hq / Hkv);
+    return R > 16 && R <= 128;
+}
+static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+static size_t qsplit_bytes(int B, int M, int Hq, int Hkv) {
+    if (!tc_rows(M, Hq, Hkv)) return 0;
+    const size_t rows = (size_t)B * M * Hq;
+    return align256(rows * 128 * 2 + rows * 4);
+}
+static size_t ws_bytes(int B, int M, int Hq, int Hkv, const Plan& p) {
+    size_t n = qsplit_bytes(B, M, Hq, Hkv);
+    if (p.num_splits > 1) n += (size_t)B * M * Hq * p.num_splits * (128 + 2) * sizeof(float);
+    return n;
 }
 
 // Opt in to the kernel's dynamic shared memory once per device (so that calls
@@ -681,8 +700,8 @@ static int launch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams
     auto kern = paged_attention_kernel<PS, FP8>;
     if (ensure_smem((const void*)kern, C::smem_bytes(std::max(C::kStages, P.KW * P.SG)))) return FP8KV_ERR_CUDA;
     dim3 grid(P.num_splits, P.Hkv, P.B);
-    kern<<<grid, (P.NT * P.KW + 1) * 32, C::smem_bytes(P.KW * P.SG), s>>>(tk, tv, P);
-    return launch_status();
+    cudaError_t e = launch_pdl(kern, grid, dim3((P.NT * P.KW + 1) * 32), C::smem_bytes(P.KW * P.SG), s, tk, tv, P);
+    return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
 }  // namespace fp8kv
@@ -704,7 +723,7 @@ extern "C" size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int
                                                        int max_seq_len, int window_left, int split_tokens) {
     Plan p;
     if (make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &p)) return (size_t)-1;
-    return ws_bytes(B, M, Hq, p);
+    return ws_bytes(B, M, Hq, Hkv, p);
 }
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -727,7 +746,7 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     if (max_seq_len < M || (int64_t)max_seq_len > (int64_t)max_pages_per_seq * page_size)
         return FP8KV_ERR_INVALID_ARG;
     if (!(sm_scale == sm_scale)) return FP8KV_ERR_INVALID_ARG;
-    const size_t need = ws_bytes(B, M, Hq, plan);
+    const size_t need = ws_bytes(B, M, Hq, Hkv, plan);
     if (need && (!workspace || workspace_bytes < need || !al16(workspace))) return FP8KV_ERR_WORKSPACE;
     if (B == 0) return FP8KV_OK;
 
@@ -742,8 +761,14 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     P.seq_lens = seq_lens;
     P.k_scale = k_scale;
     P.v_scale = v_scale;
-    P.ws_o = (float*)workspace;
-    P.ws_ml = need ? (float*)workspace + (size_t)B * M * Hq * plan.num_splits * 128 : nullptr;
+    const size_t qb = qsplit_bytes(B, M, Hq, Hkv);
+    const size_t rows = (size_t)B * M * Hq;
+    uint8_t* ws = (uint8_t*)workspace;
+    P.q_hi = qb ? ws : nullptr;
+    P.q_lo = qb ? ws + rows * 128 : nullptr;
+    P.q_mult = qb ? (float*)(ws + rows * 256) : nullptr;
+    P.ws_o = plan.num_splits > 1 ? (float*)(ws + qb) : nullptr;
+    P.ws_ml = plan.num_splits > 1 ? P.ws_o + rows * plan.num_splits * 128 : nullptr;
     P.out = (uint16_t*)out;
     P.sm_scale = sm_scale;
     P.mpps = max_pages_per_seq;
@@ -778,9 +803,9 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     cudaStream_t s = (cudaStream_t)stream;
     // up to 128 query rows per KV head on E4M3 pages, partitions of whole
     // 128-key tiles: tcgen05 kernel (one 128-row MMA tile); otherwise mma.sync
-    const bool use_tc = fp8 && P.R <= 128 && (plan.split_tokens % tc_tile_tokens()) == 0;
+    const bool use_tc = fp8 && tc_rows(M, Hq, Hkv) && (plan.split_tokens % tc_tile_tokens()) == 0;
     if (use_tc)
-        rc = launch_verify_tc(tk, tv, P, s);
+        rc = launch_attention_tc(tk, tv, P, s);
     else if (page_size == 32)
         rc = fp8 ? launch<32, true>(tk, tv, P, s) : launch<32, false>(tk, tv, P, s);
     else
@@ -788,11 +813,14 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     if (rc) return rc;
     if (plan.num_splits > 1) {
         const int64_t warps = (int64_t)B * M * Hq;
-        attn_reduce_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-            P.ws_o, P.ws_ml, seq_lens, B, M, Hq, max_pages_per_seq, page_size, window_left, plan.split_pages,
-            plan.num_splits, max_seq_len, (uint16_t*)out);
-        rc = launch_status();
-        if (rc) return rc;
+        cudaError_t e = launch_pdl(attn_reduce_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
+                                   (const float*)P.ws_o, (const float*)P.ws_ml, seq_lens, B, M, Hq,
+                                   max_pages_per_seq, page_size, window_left, plan.split_pages, plan.num_splits,
+                                   max_seq_len, (uint16_t*)out);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return FP8KV_ERR_CUDA;
+        }
     }
     char buf[256];
     if (use_tc)

@@ -12,6 +12,9 @@ struct AttnParams {
     const int32_t* seq_lens;    // [B]
     const float* k_scale;
     const float* v_scale;
+    uint8_t* q_hi;              // [B*M*Hq][128] E4M3, Q * 2^sh rounded      (tcgen05 path)
+    uint8_t* q_lo;              // [B*M*Hq][128] E4M3, the rounding residual (tcgen05 path)
+    float* q_mult;              // [B*M*Hq] logit multiplier k_scale*sm_scale*log2(e)*2^-sh
     float* ws_o;                // [B*M*Hq][num_splits][128]
     float* ws_ml;               // [B*M*Hq][num_splits][2]
     uint16_t* out;              // bf16 [B][M][Hq][128]
@@ -20,9 +23,10 @@ struct AttnParams {
     int window_left, split_pages, num_splits, page_size, max_seq_len;
 };
 
-// Host launcher of the tcgen05 verifier kernel (attention_tc.cu); returns
-// FP8KV_ERR_UNSUPPORTED when the shape is not one it implements.
-int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s);
+// Host launcher of the tcgen05 kernel (attention_tc.cu): the Q split pre-pass
+// and the attention kernel.  Returns FP8KV_ERR_UNSUPPORTED when the shape is
+// not one it implements.
+int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s);
 int status_attention_tc(unsigned int* s, int clear);
 int tc_tile_tokens();   // keys per tile of the tcgen05 kernel
 

@@ -8,11 +8,13 @@
 //
 // Q.K^T runs natively in FP8: the E4M3 K tile is the B operand straight from
 // the TMA staging buffer (its 128-byte rows with the 128-byte swizzle are the
-// K-major operand layout), and each Q row is split into two E4M3 terms after a
-// per-row power-of-two scale, q' = q * 2^sh = Q_hi + Q_lo, which is exact for
-// every bf16 element within 2^-10 of the row maximum (the rest is off by at
-// most 2^-17 of the row maximum); two accumulating MMAs give S = q'.K.  P.V
-// runs in f16: P (softmax weights) is written to tensor memory and is the A
+// K-major operand layout), and each Q row is split by a pre-pass kernel into
+// two E4M3 terms after a per-row power-of-two scale, q' = q * 2^sh = Q_hi +
+// Q_lo, which is exact for every bf16 element within 2^-10 of the row maximum
+// (the rest is off by at most 2^-17 of the row maximum); the softmax warps
+// store both rows into tensor memory (A operand) and two accumulating MMAs
+// give S = q'.K.  P.V runs
+// in f16: P (softmax weights) is written to tensor memory and is the A
 // operand, V is widened E4M3 -> f16 (exact) into a swizzled MN-major tile.
 //
 // One CTA per (partition, KV head, sequence), 16 warps:
@@ -27,6 +29,8 @@
 //                   domain, lazy O rescale (only when a row maximum grows by
 //                   more than 2^8), P to TMEM.
 // TMEM columns: Q_hi 0-31, Q_lo 32-63, S/P 2 x 128 (64-319), O 320-447.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <set>
 #include <utility>
@@ -119,6 +123,42 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f32x2_lo(uint32_t codes, float& a,
     return h;
 }
 
+// Q split pre-pass, one warp per query row (lane l: dims 4l..4l+3):
+// q' = q * 2^sh with the row maximum |q'| in [128, 256), Q_hi = e4m3(q'),
+// Q_lo = e4m3(q' - Q_hi), and the row's logit multiplier
+// k_scale * sm_scale * log2(e) * 2^-sh.
+__global__ void __launch_bounds__(256) q_split_kernel(const uint2* __restrict__ q, int64_t rows,
+                                                      const float* __restrict__ k_scale, float sm_scale,
+                                                      uint32_t* __restrict__ q_hi, uint32_t* __restrict__ q_lo,
+                                                      float* __restrict__ q_mult) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= rows) return;
+    const uint2 w = q[row * 32 + lane];
+    const float x0 = bf16_lo(w.x), x1 = bf16_hi(w.x), x2 = bf16_lo(w.y), x3 = bf16_hi(w.y);
+    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int e = 7;
+    const uint32_t ab = __float_as_uint(amax);
+    if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
+        const int be = (int)((ab >> 23) & 0xff);
+        e = be ? be - 127 : -127;
+    }
+    const int sh = max(-100, min(100, 7 - e));
+    const float scale = ldexpf(1.0f, sh);
+    const float a0 = x0 * scale, a1 = x1 * scale, a2 = x2 * scale, a3 = x3 * scale;
+    const uint32_t h01 = e4m3x2(a0, a1), h23 = e4m3x2(a2, a3);
+    float d0, d1, d2, d3;
+    e4m3x2_to_f32x2_lo(h01, d0, d1);
+    e4m3x2_to_f32x2_lo(h23, d2, d3);
+    q_hi[row * 32 + lane] = h01 | (h23 << 16);
+    q_lo[row * 32 + lane] = e4m3x2(a0 - d0, a1 - d1) | (e4m3x2(a2 - d2, a3 - d3) << 16);
+    if (lane == 0) q_mult[row] = (*k_scale) * sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+}
+
 template <int PS>
 __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
@@ -134,6 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
 
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
     const int L = P.seq_lens[b];
     if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
         if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
@@ -187,11 +229,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
+        const uint64_t policy = policy_evict_first();
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
-        const uint64_t policy = policy_evict_first();
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         int issued = 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
@@ -339,58 +381,23 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int m = rr / P.G;
         const int p_r = L - P.M + m;
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
-        float mult;
+        const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
+        const float mult = P.q_mult[row_idx];
+        const bool pad = r >= P.R;                          // rows past M*G: zero weight
         {
-            // q' = q * 2^sh with the row maximum in [128, 256); half 0 stores
-            // Q_hi = e4m3(q'), half 1 stores Q_lo = e4m3(q' - Q_hi)
-            float amax = 0.f;
-            const uint4* src = (const uint4*)(P.q + (((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G) * 128);
+            // the pre-split Q row: half 0 stores Q_hi, half 1 Q_lo (A operand of Q.K^T)
+            const uint4* src = (const uint4*)((half == 0 ? P.q_hi : P.q_lo) + row_idx * 128);
+            uint32_t qw[32];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const uint4 w = (r < P.R) ? src[u] : make_uint4(0, 0, 0, 0);
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.x)), fabsf(bf16_hi(w.x))),
-                                         fmaxf(fabsf(bf16_lo(w.y)), fabsf(bf16_hi(w.y)))));
-                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(w.z)), fabsf(bf16_hi(w.z))),
-                                         fmaxf(fabsf(bf16_lo(w.w)), fabsf(bf16_hi(w.w)))));
+            for (int u = 0; u < 8; ++u) {
+                const uint4 w = pad ? make_uint4(0, 0, 0, 0) : src[u];
+                qw[4 * u] = w.x;
+                qw[4 * u + 1] = w.y;
+                qw[4 * u + 2] = w.z;
+                qw[4 * u + 3] = w.w;
             }
-            int e = 7;
-            const uint32_t ab = __float_as_uint(amax);
-            if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
-                const int be = (int)((ab >> 23) & 0xff);
-                e = be ? be - 127 : -127;
-            }
-            const int sh = max(-100, min(100, 7 - e));
-            const float scale = ldexpf(1.0f, sh);
-#pragma unroll 1
-            for (int hh = 0; hh < 2; ++hh) {   // 64 dims per pass: 16 TMEM columns
-                uint32_t qw[32], outw[16];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint4 w = (r < P.R) ? src[8 * hh + u] : make_uint4(0, 0, 0, 0);
-                    qw[4 * u] = w.x;
-                    qw[4 * u + 1] = w.y;
-                    qw[4 * u + 2] = w.z;
-                    qw[4 * u + 3] = w.w;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const uint32_t w0 = qw[2 * j], w1 = qw[2 * j + 1];
-                    const float a0 = bf16_lo(w0) * scale, a1 = bf16_hi(w0) * scale;
-                    const float a2 = bf16_lo(w1) * scale, a3 = bf16_hi(w1) * scale;
-                    const uint32_t h01 = e4m3x2(a0, a1), h23 = e4m3x2(a2, a3);
-                    if (half == 0) {
-                        outw[j] = h01 | (h23 << 16);
-                    } else {
-                        float d0, d1, d2, d3;
-                        e4m3x2_to_f32x2_lo(h01, d0, d1);
-                        e4m3x2_to_f32x2_lo(h23, d2, d3);
-                        outw[j] = e4m3x2(a0 - d0, a1 - d1) | (e4m3x2(a2 - d2, a3 - d3) << 16);
-                    }
-                }
-                tmem_st_x16(lane_base + (half == 0 ? TM_QH : TM_QL) + 16 * hh, outw);
-            }
+            tmem_st_x32(lane_base + (half == 0 ? TM_QH : TM_QL), qw);
             tmem_wait_st();
-            mult = (*P.k_scale) * P.sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
         }
         fence_before();
         __syncwarp();
@@ -414,10 +421,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 uint32_t sv[64];
                 tmem_ld_x64(scol, sv);
                 tmem_wait_ld();
-                if ((k0 + 63 > pmin) || (k0 < lomax)) {
+                if ((k0 + 63 > pmin) || (k0 < lomax) || pad) {
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        if (k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
+                        if (pad || k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
                 }
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -493,7 +500,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         if (ok && active) {
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const float vs = *P.v_scale;
-            const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
             const bool direct = nsplit_b == 1;
             const float f = direct ? vs / l_tot : vs;
 #pragma unroll 1
@@ -542,8 +548,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
 
 int tc_tile_tokens() { return tc::NK; }
 
-int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
-    if (P.R > 128) return FP8KV_ERR_UNSUPPORTED;
+int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
+    if (P.R > 128 || P.R <= 16 || !P.q_hi) return FP8KV_ERR_UNSUPPORTED;
     if ((P.split_pages * P.page_size) % tc::NK) return FP8KV_ERR_UNSUPPORTED;
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
@@ -559,12 +565,18 @@ int launch_verify_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnPar
             done.insert({dev, kern});
         }
     }
+    const int64_t rows = (int64_t)P.B * P.M * P.Hq;
+    cudaError_t e = launch_pdl(tc::q_split_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s,
+                               (const uint2*)P.q, rows, P.k_scale, P.sm_scale, (uint32_t*)P.q_hi,
+                               (uint32_t*)P.q_lo, P.q_mult);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return FP8KV_ERR_CUDA;
+    }
     dim3 grid(P.num_splits, P.Hkv, P.B);
-    if (P.page_size == 32)
-        tc::attention_tc_kernel<32><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
-    else
-        tc::attention_tc_kernel<64><<<grid, tc::THREADS, tc::SMEM, s>>>(tk, tv, P);
-    return launch_status();
+    e = launch_pdl(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
+                   dim3(tc::THREADS), tc::SMEM, s, tk, tv, P);
+    return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
 }  // namespace fp8kv

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) insert_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
     int T, int Hkv, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots, int page_size) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)T * Hkv * 16) return;
     const int chunk = (int)(i & 15);
@@ -73,6 +75,8 @@ __global__ void __launch_bounds__(256) norm_rope_insert_kernel(
     const int64_t* __restrict__ slots, int T, int Hq, int Hkv, const float* __restrict__ k_scale,
     const float* __restrict__ v_scale, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
     int64_t num_slots, int page_size) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int heads = Hq + Hkv;
@@ -194,15 +198,11 @@ extern "C" int fp8kv_cache_insert(const void* k, const void* v, const int64_t* s
     if (blocks > 0x7fffffff) return FP8KV_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     const int64_t num_slots = (int64_t)num_pages * page_size;
-    if (cache_dtype == FP8KV_CACHE_E4M3)
-        insert_kernel<true><<<(unsigned)blocks, threads, 0, s>>>(
-            (const uint4*)k, (const uint4*)v, slot_mapping, T, Hkv, k_scale, v_scale,
-            (uint8_t*)k_cache, (uint8_t*)v_cache, num_slots, page_size);
-    else
-        insert_kernel<false><<<(unsigned)blocks, threads, 0, s>>>(
-            (const uint4*)k, (const uint4*)v, slot_mapping, T, Hkv, k_scale, v_scale,
-            (uint8_t*)k_cache, (uint8_t*)v_cache, num_slots, page_size);
-    return launch_status();
+    cudaError_t e = launch_pdl(cache_dtype == FP8KV_CACHE_E4M3 ? insert_kernel<true> : insert_kernel<false>,
+                               dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)k, (const uint4*)v,
+                               slot_mapping, T, Hkv, k_scale, v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache,
+                               num_slots, page_size);
+    return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
 extern "C" int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const void* v,
@@ -227,12 +227,12 @@ extern "C" int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const voi
     const int64_t warps = (int64_t)T * (Hq + Hkv);
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7fffffff) return FP8KV_ERR_UNSUPPORTED;
-    norm_rope_insert_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(
-        (const uint2*)q, (const uint2*)k, (const uint2*)v, positions, (const uint2*)q_norm_w,
-        (const uint2*)k_norm_w, eps, (const float4*)cos_sin, max_pos, (uint2*)q_out, slot_mapping, T, Hq,
-        Hkv, k_scale, v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache, (int64_t)num_pages * page_size,
-        page_size);
-    return launch_status();
+    cudaError_t e = launch_pdl(norm_rope_insert_kernel, dim3((unsigned)blocks), dim3(256), 0, (cudaStream_t)stream,
+                               (const uint2*)q, (const uint2*)k, (const uint2*)v, positions, (const uint2*)q_norm_w,
+                               (const uint2*)k_norm_w, eps, (const float4*)cos_sin, max_pos, (uint2*)q_out,
+                               slot_mapping, T, Hq, Hkv, k_scale, v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache,
+                               (int64_t)num_pages * page_size, page_size);
+    return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
 extern "C" int fp8kv_e4m3_encode_bits(uint32_t first, size_t n, uint8_t* out, void* stream) {
