@@ -280,28 +280,39 @@ def capture_step_graphs(w: Workload, stream):
     return graphs
 
 
-def dominant_kernel(w: Workload, stream, reps=30):
-    """Average duration of the attention call (partial kernel + reduce) on the
-    layer kind with the most bytes, launched alone between CUDA events on its
-    own stream, rotating cache copies / layers so the cache reads come from HBM."""
+def dominant_kernel(w: Workload, stream, reps=24):
+    """Average device duration of the attention call (partial kernel + reduce) on
+    the layer kind with the most bytes.  `reps` calls, rotating over cache copies
+    and layers so the cache reads come from HBM, are captured in one CUDA graph;
+    graph replays are timed with CUDA events on the launching stream, so host
+    launch overhead stays outside the figure."""
     cands = [(l.attn_bytes(), li) for li, l in enumerate(w.copies[0])]
     top = max(b for b, _ in cands)
     idx = [li for b, li in cands if b == top]
     layers = [c[li] for c in w.copies for li in idx]
-    evs = []
     with torch.cuda.stream(stream):
         for i in range(3):
             layers[i % len(layers)].attend(w.ws)
-        for i in range(reps):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            layers[i % len(layers)].attend(w.ws)
-            b.record(stream)
-            evs.append((a, b))
     torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(reps):
+            layers[i % len(layers)].attend(w.ws)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    per_call = []
+    for _ in range(7):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        b.synchronize()
+        per_call.append(a.elapsed_time(b) / reps)
+    del g
     from verify_attention_gb300 import fp8kv
-    return top, ms / 1e3, flops_of(layers[0]), fp8kv.fp8kv_last_dispatch()
+    return top, statistics.median(per_call) / 1e3, flops_of(layers[0]), fp8kv.fp8kv_last_dispatch()
 
 
 def flops_of(layer):

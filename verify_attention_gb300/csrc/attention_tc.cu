@@ -116,13 +116,6 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_f32x2_lo(uint32_t codes, float& a, float& b) {
-    const uint32_t h = e4m3x2_to_f16x2(codes);
-    a = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
-    b = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
-    return h;
-}
-
 // Q split pre-pass, one warp per query row (lane l: dims 4l..4l+3):
 // q' = q * 2^sh with the row maximum |q'| in [128, 256), Q_hi = e4m3(q'),
 // Q_lo = e4m3(q' - Q_hi), and the row's logit multiplier
@@ -149,13 +142,10 @@ __global__ void __launch_bounds__(256) q_split_kernel(const uint2* __restrict__ 
     }
     const int sh = max(-100, min(100, 7 - e));
     const float scale = ldexpf(1.0f, sh);
-    const float a0 = x0 * scale, a1 = x1 * scale, a2 = x2 * scale, a3 = x3 * scale;
-    const uint32_t h01 = e4m3x2(a0, a1), h23 = e4m3x2(a2, a3);
-    float d0, d1, d2, d3;
-    e4m3x2_to_f32x2_lo(h01, d0, d1);
-    e4m3x2_to_f32x2_lo(h23, d2, d3);
-    q_hi[row * 32 + lane] = h01 | (h23 << 16);
-    q_lo[row * 32 + lane] = e4m3x2(a0 - d0, a1 - d1) | (e4m3x2(a2 - d2, a3 - d3) << 16);
+    uint32_t hi, lo;
+    e4m3_split4(x0 * scale, x1 * scale, x2 * scale, x3 * scale, hi, lo);
+    q_hi[row * 32 + lane] = hi;
+    q_lo[row * 32 + lane] = lo;
     if (lane == 0) q_mult[row] = (*k_scale) * sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
 }
 
@@ -383,7 +373,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
         const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
         const float mult = P.q_mult[row_idx];
-        const bool pad = r >= P.R;                          // rows past M*G: zero weight
+        // rows past M*G get Q = 0: their (unused) weights stay finite and their
+        // lanes take the same unmasked path as the real rows
+        const bool pad = r >= P.R;
         {
             // the pre-split Q row: half 0 stores Q_hi, half 1 Q_lo (A operand of Q.K^T)
             const uint4* src = (const uint4*)((half == 0 ? P.q_hi : P.q_lo) + row_idx * 128);
@@ -421,10 +413,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 uint32_t sv[64];
                 tmem_ld_x64(scol, sv);
                 tmem_wait_ld();
-                if ((k0 + 63 > pmin) || (k0 < lomax) || pad) {
+                if ((k0 + 63 > pmin) || (k0 < lomax)) {
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        if (pad || k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
+                        if (k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
                 }
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll

@@ -42,6 +42,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
     return r;
 }
 
+// Two E4M3 codes (bits 0..15) -> two fp32 values, exact.
+__device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float& hi) {
+    const uint32_t h = e4m3x2_to_f16x2(codes);
+    lo = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+    hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+}
+
+// Four fp32 values (already scaled so the row maximum lies in [128, 256))
+// -> their E4M3 leading terms x_hi = e4m3(x) and residual terms
+// x_lo = e4m3(x - x_hi), four codes per word (element 0 in bits 0..7).
+// x_hi + x_lo reproduces x exactly for every bf16 x of at least 2^-2
+// (residuals of at most four significant bits, all above the E4M3
+// subnormal step 2^-9); below that the pair is off by at most 2^-10.
+__device__ __forceinline__ void e4m3_split4(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
+    const uint32_t h01 = e4m3x2(x0, x1), h23 = e4m3x2(x2, x3);
+    float d0, d1, d2, d3;
+    e4m3x2_to_f32x2(h01, d0, d1);
+    e4m3x2_to_f32x2(h23, d2, d3);
+    hi = h01 | (h23 << 16);
+    lo = e4m3x2(x0 - d0, x1 - d1) | (e4m3x2(x2 - d2, x3 - d3) << 16);
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -76,6 +98,16 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
     asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D += A * B, m16n8k32, E4M3 x E4M3, fp32 accumulate; A row-major, B
+// column-major; each register holds four consecutive k elements.
+__device__ __forceinline__ void mma_e4m3(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
