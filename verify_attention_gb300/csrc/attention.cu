@@ -21,8 +21,9 @@
 //    Q is scaled by a per-row power of two into f16 range (exact for bf16);
 //    the BF16 cache runs the same loop in bf16;
 //  * online softmax in fp32 (log2 domain) with quad shuffles;
-//  * when the M x G rows fit one row tile (decode), up to four key groups of
-//    warps split the pages of a partition and are merged through shared
+//  * when the M x G rows fit one row tile (decode), six key groups of warps
+//    split the pages of a partition, each with two or more stages in flight,
+//    one CTA per SM (paged_decode_kernel); they are merged through shared
 //    memory at the end;
 //  * one partition per sequence writes bf16 output directly; otherwise each
 //    partition writes (max, sum, unnormalised output) and attn_reduce_kernel
@@ -37,15 +38,23 @@ namespace fp8kv {
 int status_attention(unsigned int* s, int clear) { return read_status(s, clear); }
 
 constexpr int kMaxRowTiles = 9;          // M*G <= 144
-// Bytes of K/V stages per CTA and key groups of the decode shape (one row
-// tile); overridable at build time for tuning sweeps.
+// Bytes of K/V stages per CTA for several row tiles; for the decode shape
+// (one row tile) the key groups, their stage budget and the register cap of
+// the decode kernel.  Overridable at build time for tuning sweeps.
 #ifndef FP8KV_STAGE_KB
 #define FP8KV_STAGE_KB 96
 #endif
 #ifndef FP8KV_DECODE_KEY_GROUPS
-#define FP8KV_DECODE_KEY_GROUPS 4
+#define FP8KV_DECODE_KEY_GROUPS 6
+#endif
+#ifndef FP8KV_DECODE_STAGE_KB
+#define FP8KV_DECODE_STAGE_KB 200
+#endif
+#ifndef FP8KV_DECODE_REGS
+#define FP8KV_DECODE_REGS 200
 #endif
 constexpr int kStageBudget = FP8KV_STAGE_KB * 1024;
+constexpr int kDecodeStageBudget = FP8KV_DECODE_STAGE_KB * 1024;
 
 template <int PS, bool FP8>
 struct Cfg {
@@ -73,8 +82,8 @@ __device__ __forceinline__ RowPos row_pos(int r, int R, int G, int L, int M, int
 __device__ __forceinline__ uint32_t swz(int row, int ch) { return row * 128 + (((ch ^ row) & 7) << 4); }
 
 template <int PS, bool FP8>
-__global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
+__device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                               const AttnParams& P) {
     using C = Cfg<PS, FP8>;
     const int S = P.KW * P.SG;                                  // stages in use
     extern __shared__ uint8_t smem_raw[];
@@ -495,6 +504,23 @@ __global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_ke
     }
 }
 
+// Several row tiles (verifier rows on a BF16 cache, or more than 128 rows):
+// up to ten warps, registers capped so that one CTA fits an SM.
+template <int PS, bool FP8>
+__global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
+    attention_body<PS, FP8>(tm_k, tm_v, P);
+}
+
+// One row tile (decode): a handful of key-group warps, each with two or more
+// stages in flight, one CTA per SM; at most two warps per SM sub-partition,
+// so the register cap can be high enough to keep every fragment resident.
+template <int PS, bool FP8>
+__global__ void __maxnreg__(FP8KV_DECODE_REGS) paged_decode_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
+    attention_body<PS, FP8>(tm_k, tm_v, P);
+}
+
 // One warp per output row (b, m, h): combine the partitions through their
 // log-sum-exp, O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p.
 __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restrict__ ws_o,
@@ -639,13 +665,18 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
     if (split_tokens > 0) {
         sp = split_tokens / PS;
     } else {
-        // about two partitions per SM over all (sequence, head) units, with
-        // at least 1024 keys per partition: per-CTA set-up and the partial
-        // write-back make short partitions expensive
+        // one (decode: a single row tile, one CTA per SM) or two partitions
+        // per SM over all (sequence, head) units, with at least 1024 keys per
+        // partition: per-CTA set-up and the partial write-back make short
+        // partitions expensive
         const int64_t units = (int64_t)max(B, 1) * Hkv;
-        const int64_t target = 2LL * num_sms();
+        const int64_t target = (M * (Hq / Hkv) <= 16 ? 1LL : 2LL) * num_sms();
         const int per = (int)std::max<int64_t>(1, (target + units - 1) / units);
         sp = max(ceil_div(pages, per), 1024 / PS);
+        // with many units and long sequences, at least four partitions per
+        // sequence keep the longest ones from holding an SM alone at the end
+        // of the launch (sequence lengths are only known on the device)
+        if (ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
     }
     sp = max(1, min(sp, pages));
     // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
@@ -697,8 +728,10 @@ static int ensure_smem(const void* kern, int bytes) {
 template <int PS, bool FP8>
 static int launch(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
     using C = Cfg<PS, FP8>;
-    auto kern = paged_attention_kernel<PS, FP8>;
-    if (ensure_smem((const void*)kern, C::smem_bytes(std::max(C::kStages, P.KW * P.SG)))) return FP8KV_ERR_CUDA;
+    const bool decode = P.NT == 1;
+    auto kern = decode ? paged_decode_kernel<PS, FP8> : paged_attention_kernel<PS, FP8>;
+    const int max_stages = decode ? kDecodeStageBudget / C::kStageBytes : C::kStages;
+    if (ensure_smem((const void*)kern, C::smem_bytes(std::max(max_stages, P.KW * P.SG)))) return FP8KV_ERR_CUDA;
     dim3 grid(P.num_splits, P.Hkv, P.B);
     cudaError_t e = launch_pdl(kern, grid, dim3((P.NT * P.KW + 1) * 32), C::smem_bytes(P.KW * P.SG), s, tk, tv, P);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
@@ -784,9 +817,12 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
         // idle; each group keeps at least two stages in flight when it can
         const int stages = page_size == 32 ? (fp8 ? Cfg<32, true>::kStages : Cfg<32, false>::kStages)
                                            : (fp8 ? Cfg<64, true>::kStages : Cfg<64, false>::kStages);
+        const int elem_b = fp8 ? 1 : 2;
+        const int dstages = kDecodeStageBudget / (2 * page_size * 128 * elem_b);
         int kw = P.NT == 1 ? FP8KV_DECODE_KEY_GROUPS : (P.NT == 2 ? 2 : 1);
-        kw = std::max(1, std::min(kw, stages));
-        int sg = std::max(1, stages / kw);
+        const int avail = P.NT == 1 ? dstages : stages;
+        kw = std::max(1, std::min(kw, avail));
+        int sg = std::max(1, avail / kw);
         // the epilogue merges the key groups' rows through the stage ring
         const int elem = fp8 ? 1 : 2, stage_bytes = 2 * page_size * 128 * elem;
         const int merge = kw * P.NT * 16 * 132 * 4;

@@ -1,6 +1,6 @@
-// attention_tc.cu -- paged decode / verifier attention on the 5th-generation
-// tensor cores (tcgen05) for up to 128 query rows per KV head: M = 1 decode
-// (9 rows) and the M = 12 verifier (108 rows) of "Laguna S 2.1 INT4 --
+// attention_tc.cu -- paged verifier attention on the 5th-generation tensor
+// cores (tcgen05) for 17 to 128 query rows per KV head (M x G rows; the
+// M = 12 verifier has 108) of "Laguna S 2.1 INT4 --
 // calibrated FP8 KV on Intel B70" ("Contract"; "Initial optimization order",
 // item 2: exact q1/M12 paged attention) over the E4M3 cache ("Laguna S 2.1
 // KV-cache precision decision", property table: "scale/dequantize or use native
@@ -13,9 +13,9 @@
 // Q_lo, which is exact for every bf16 element within 2^-10 of the row maximum
 // (the rest is off by at most 2^-17 of the row maximum); the softmax warps
 // store both rows into tensor memory (A operand) and two accumulating MMAs
-// give S = q'.K.  P.V runs
-// in f16: P (softmax weights) is written to tensor memory and is the A
-// operand, V is widened E4M3 -> f16 (exact) into a swizzled MN-major tile.
+// give S = q'.K.  P.V runs in f16: P (softmax weights) is written to tensor
+// memory and is the A operand, V is widened E4M3 -> f16 (exact) into a
+// swizzled MN-major tile.  Rows past M x G (up to 128) carry Q = 0.
 //
 // One CTA per (partition, KV head, sequence), 16 warps:
 //   warp 0          TMA producer (128-key tiles: K and V E4M3, 2 or 4 pages);
