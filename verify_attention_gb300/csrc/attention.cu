@@ -21,7 +21,7 @@
 //    Q is scaled by a per-row power of two into f16 range (exact for bf16);
 //    the BF16 cache runs the same loop in bf16;
 //  * online softmax in fp32 (log2 domain) with quad shuffles;
-//  * when the M x G rows fit one row tile (decode), six key groups of warps
+//  * when the M x G rows fit one row tile (decode), seven key groups of warps
 //    split the pages of a partition, each with two or more stages in flight,
 //    one CTA per SM (paged_decode_kernel); they are merged through shared
 //    memory at the end;
@@ -45,10 +45,10 @@ constexpr int kMaxRowTiles = 9;          // M*G <= 144
 #define FP8KV_STAGE_KB 96
 #endif
 #ifndef FP8KV_DECODE_KEY_GROUPS
-#define FP8KV_DECODE_KEY_GROUPS 6
+#define FP8KV_DECODE_KEY_GROUPS 7
 #endif
 #ifndef FP8KV_DECODE_STAGE_KB
-#define FP8KV_DECODE_STAGE_KB 200
+#define FP8KV_DECODE_STAGE_KB 224
 #endif
 #ifndef FP8KV_DECODE_REGS
 #define FP8KV_DECODE_REGS 200
