@@ -158,7 +158,23 @@ def test_dispatch_marker_reports_variant():
     kc, vc, ks, vs = gpu_caches(case)
     gpu_attention(case, kc, vc, ks, vs, split_tokens=512)
     d = fp8kv().fp8kv_last_dispatch()
-    assert "ps=64" in d and "e4m3" in d and "splits=4" in d
+    assert d.startswith("paged_decode_mma") and "ps=64" in d and "e4m3" in d and "splits=4" in d, d
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+def test_decode_kernel_key_groups(ps, dtype):
+    """M = 1 rows run on the decode kernel (several key groups, each with its
+    own stages); partitions long enough for every group to take several pages,
+    a ragged last page, and a partition shorter than the group count."""
+    case = gen.layer_case(8750 + ps, [ps * 37 + 5, 3 * ps - 1], 1, ps)
+    kc, vc, ks, vs = gpu_caches(case, cache_dtype=dtype)
+    okc, ovc = oracle_caches(case, cache_dtype=dtype)
+    ref = oracle_attention(case, okc, ovc, cache_dtype=dtype)
+    for st in (0, ps * 16, ps * 2):
+        out = gpu_attention(case, kc, vc, ks, vs, split_tokens=st)
+        assert fp8kv().fp8kv_last_dispatch().startswith("paged_decode_mma")
+        assert_close(out, ref, f"ps={ps} {dtype} split={st}")
 
 
 # ------------------------------------------------------------ the configs

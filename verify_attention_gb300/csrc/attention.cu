@@ -93,7 +93,18 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_cons = P.NT * P.KW;
+    const int SG = P.SG;
     pdl_launch_dependents();
+    // barrier set-up reads no memory an earlier kernel may write: it overlaps
+    // the tail of the previous kernel in the stream
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);
+            mbar_init(smem_u32(&bars[S + s]), P.NT);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
     pdl_wait();
     const int L = P.seq_lens[b];
     if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
@@ -115,15 +126,6 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
     // to group i % KW, its j-th page (j = i / KW) to stage g*SG + j % SG, use
     // j / SG of that stage: every wait below is for the next phase of a barrier
     // only its own consumer advances, so a parity test can never pass early.
-    const int SG = P.SG;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&bars[s]), 1);
-            mbar_init(smem_u32(&bars[S + s]), P.NT);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
 
     if (warp == n_cons) {
         // ------------------------------------------------------------ producer
@@ -861,15 +863,16 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     char buf[256];
     if (use_tc)
         snprintf(buf, sizeof buf,
-                 "attention_tc<ps=%d,e4m3> rows=%d tile=128x128 splits=%d split_tokens=%d grid=%dx%dx%d threads=448 "
+                 "attention_tc<ps=%d,e4m3> rows=%d tile=128x128 splits=%d split_tokens=%d grid=%dx%dx%d threads=%d "
                  "reduce=%d",
-                 page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B,
+                 page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B, tc_threads(),
                  plan.num_splits > 1 ? 1 : 0);
     else
         snprintf(buf, sizeof buf,
-                 "paged_attention_mma<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "
+                 "%s<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "
                  "split_tokens=%d grid=%dx%dx%d threads=%d reduce=%d",
-                 page_size, fp8 ? "e4m3" : "bf16", P.R, P.NT, P.KW, P.SG, plan.num_splits, plan.split_tokens,
+                 P.NT == 1 ? "paged_decode_mma" : "paged_attention_mma", page_size, fp8 ? "e4m3" : "bf16", P.R,
+                 P.NT, P.KW, P.SG, plan.num_splits, plan.split_tokens,
                  plan.num_splits, Hkv, B, (P.NT * P.KW + 1) * 32, plan.num_splits > 1 ? 1 : 0);
     set_dispatch(buf);
     return FP8KV_OK;

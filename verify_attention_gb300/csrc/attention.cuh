@@ -29,5 +29,6 @@ struct AttnParams {
 int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s);
 int status_attention_tc(unsigned int* s, int clear);
 int tc_tile_tokens();   // keys per tile of the tcgen05 kernel
+int tc_threads();       // threads per CTA of the tcgen05 kernel
 
 }  // namespace fp8kv

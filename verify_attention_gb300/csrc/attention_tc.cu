@@ -53,6 +53,10 @@ constexpr int VBUFS = 3;                        // f16 V tiles
 constexpr int VBUF_BYTES = NK * 256;            // 32 KiB
 constexpr int XCH_BYTES = 3 * 2 * 128 * 4;      // [tile parity 0, parity 1, row sums][half][row]
 constexpr int SMEM = STAGES * STG_BYTES + VBUFS * VBUF_BYTES + XCH_BYTES + 1024 + 512;
+// epilogue: one staged half row (<= 256 B) per (half, row), padded against
+// bank conflicts, in the staging buffers (free once the last tile is consumed)
+constexpr int EPI_STRIDE = 272;
+static_assert(2 * 128 * EPI_STRIDE <= STAGES * STG_BYTES, "epilogue staging exceeds the stage ring");
 constexpr uint32_t TM_QH = 0, TM_QL = 32, TM_S = 64, TM_O = 320, TM_COLS = 512;
 constexpr int WARPS = 16, THREADS = WARPS * 32;
 constexpr int CONV_WARPS = 6, CONV_THREADS = CONV_WARPS * 32;
@@ -165,26 +169,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
-    pdl_wait();
-    const int L = P.seq_lens[b];
-    if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
-        if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
-        return;
-    }
-    const int lo0 = (P.window_left >= 0) ? max(0, L - P.M - P.window_left) : 0;
-    const int first_page = lo0 / PS, last_page = (L - 1) / PS;
-    const int nsplit_b = (last_page - first_page + P.split_pages) / P.split_pages;
-    if (nsplit_b > P.num_splits) {
-        if (threadIdx.x == 0 && split == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
-        return;
-    }
-    if (split >= nsplit_b) return;
-    const int page_begin = first_page + split * P.split_pages;
-    const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
-    constexpr int PPT = NK / PS;                            // pages per tile
-    const int n_tiles = (n_pages + PPT - 1) / PPT;
-    const int k_begin = page_begin * PS;
 
+    // Set-up that reads no memory an earlier kernel may write: it overlaps
+    // the tail of the previous kernel in the stream.
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar(B_STG_FULL + s), 1);
@@ -210,20 +197,43 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                      "r"(TM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
     }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    pdl_wait();
+    const int L = P.seq_lens[b];
+    bool run = true;                                        // uniform over the CTA
+    if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
+        if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+        run = false;
+    }
+    const int lo0 = (P.window_left >= 0) ? max(0, L - P.M - P.window_left) : 0;
+    const int first_page = lo0 / PS, last_page = (L - 1) / PS;
+    const int nsplit_b = (last_page - first_page + P.split_pages) / P.split_pages;
+    if (run && nsplit_b > P.num_splits) {
+        if (threadIdx.x == 0 && split == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+        run = false;
+    }
+    if (split >= nsplit_b) run = false;
+    const int page_begin = first_page + split * P.split_pages;
+    const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
+    constexpr int PPT = NK / PS;                            // pages per tile
+    const int n_tiles = (n_pages + PPT - 1) / PPT;
+    const int k_begin = page_begin * PS;
     bool ok = true;
 
-    if (warp == 0) {
+    if (!run) {
+        // no keys of this sequence fall in this partition (or bad input)
+    } else if (warp == 0) {
         // ---------------------------------------------------------- producer
         const uint64_t policy = policy_evict_first();
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         int issued = 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
@@ -373,6 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
         const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
         const float mult = P.q_mult[row_idx];
+        const float vs = *P.v_scale;
         // rows past M*G get Q = 0: their (unused) weights stay finite and their
         // lanes take the same unmasked path as the real rows
         const bool pad = r >= P.R;
@@ -491,34 +502,43 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         }
         if (ok && active) {
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
-            const float vs = *P.v_scale;
             const bool direct = nsplit_b == 1;
             const float f = direct ? vs / l_tot : vs;
+            // This thread's half row (64 dims: bf16 output or fp32 partial)
+            // goes through the free staging buffers to one bulk copy: stores
+            // straight from the row-per-thread TMEM layout would touch a
+            // different row, hence cache line, in every lane.
+            uint8_t* row_stage = stg + (half * 128 + r) * EPI_STRIDE;
 #pragma unroll 1
             for (int c = 0; c < 64; c += 32) {
                 uint32_t ov[32];
                 tmem_ld_x32(lane_base + TM_O + 64 * half + c, ov);
                 tmem_wait_ld();
-                if (r < P.R) {
-                    const int d0 = 64 * half + c;
-                    if (direct) {
-                        uint4* dst = (uint4*)(P.out + row_idx * 128 + d0);
+                if (direct) {
+                    uint4* dst = (uint4*)(row_stage + c * 2);
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            dst[v4] = make_uint4(
-                                pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * f, __uint_as_float(ov[8 * v4 + 1]) * f),
-                                pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
-                                pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
-                                pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
-                    } else {
-                        float4* dst = (float4*)(P.ws_o + (row_idx * P.num_splits + split) * 128 + d0);
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(
+                            pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * f, __uint_as_float(ov[8 * v4 + 1]) * f),
+                            pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
+                            pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
+                            pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
+                } else {
+                    float4* dst = (float4*)(row_stage + c * 4);
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * f, __uint_as_float(ov[4 * v4 + 1]) * f,
-                                                  __uint_as_float(ov[4 * v4 + 2]) * f,
-                                                  __uint_as_float(ov[4 * v4 + 3]) * f);
-                    }
+                    for (int v4 = 0; v4 < 8; ++v4)
+                        dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * f, __uint_as_float(ov[4 * v4 + 1]) * f,
+                                              __uint_as_float(ov[4 * v4 + 2]) * f, __uint_as_float(ov[4 * v4 + 3]) * f);
                 }
+            }
+            if (r < P.R) {
+                fence_proxy_async();        // the staged row, written by this thread, to the bulk copy
+                if (direct)
+                    bulk_store(P.out + row_idx * 128 + 64 * half, smem_u32(row_stage), 128);
+                else
+                    bulk_store(P.ws_o + (row_idx * P.num_splits + split) * 128 + 64 * half, smem_u32(row_stage), 256);
+                bulk_commit();
+                bulk_wait_read();
             }
             if (r < P.R && !direct && half == 0) {
                 P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
@@ -539,6 +559,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
 }  // namespace tc
 
 int tc_tile_tokens() { return tc::NK; }
+int tc_threads() { return tc::THREADS; }
 
 int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
     if (P.R > 128 || P.R <= 16 || !P.q_hi) return FP8KV_ERR_UNSUPPORTED;
