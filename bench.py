@@ -425,13 +425,18 @@ def cpu_baseline(name, page_size, target_s=12.0):
 # -------------------------------------------------------------------- main
 
 def dist_setup():
+    """One process per GPU (torchrun env); NCCL on GPUs, gloo without one
+    (the host-side logic is the same; the CPU tests use gloo)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     return ws, rank, local
 
 
@@ -445,9 +450,16 @@ def max_over_ranks(x, ws):
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_gbs(ws, bytes_per_rank_step, step_s):
+    """Replicas: every rank runs the same step; the job moves ws times one
+    rank's bytes in the slowest rank's time."""
+    return ws * bytes_per_rank_step / step_s / 1e9
 
 
 def run_reference(args):
@@ -521,7 +533,7 @@ def main():
 
     step_bytes = w.bytes_per_step()
     step_s = secs / args.steps
-    value = ws * step_bytes / step_s / 1e9
+    value = whole_job_gbs(ws, step_bytes, step_s)
 
     dom_bytes, dom_s, dom_flops, dispatch = dominant_kernel(w, stream)
     achieved = dom_bytes / dom_s / 1e9

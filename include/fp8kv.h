@@ -140,12 +140,11 @@ int fp8kv_paged_attention_plan(int B, int M, int Hq, int Hkv, int D, int page_si
                                int max_seq_len, int window_left, int split_tokens,
                                int* num_splits, int* split_tokens_out);
 
-/* Workspace bytes fp8kv_paged_attention needs for the same arguments: the
- * split-KV partials when a sequence spans several partitions, plus, for 17 to
- * 128 query rows per KV head, an E4M3 split of Q (two 128-byte rows and a
- * multiplier per query row) read by the tensor-memory kernel.  The size does
- * not depend on the cache dtype.  0 when neither applies; (size_t)-1 on bad
- * arguments. */
+/* Workspace bytes fp8kv_paged_attention needs for the same arguments: room
+ * for the split-KV partials (fp32 output, max and sum per query row and
+ * partition) when a sequence spans several partitions, counted even when the
+ * call combines them on chip.  The size does not depend on the cache dtype.
+ * 0 for one partition; (size_t)-1 on bad arguments. */
 size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D,
                                             int page_size, int max_seq_len, int window_left,
                                             int split_tokens);
@@ -167,7 +166,10 @@ size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D
  *     out[b][m][h] = softmax_j( (q . Kd_j) * sm_scale ) . Vd      (rounded to bf16)
  * computed with fp32 accumulation.  Long contexts are cut into partitions of
  * split_tokens keys whose partial (max, sum, unnormalised output) are combined
- * by a reduce kernel through their log-sum-exp.
+ * through their log-sum-exp: by a reduce kernel over workspace partials, or,
+ * for one sequence (B = 1) of 17 to 128 rows per KV head on an E4M3 cache in
+ * at most 8 partitions, on chip by the partitions of a KV head running as one
+ * thread-block cluster (fp8kv_last_dispatch reports "cluster=N").
  *
  *   q            (device) bf16 [B][M][Hq][D]
  *   k_cache, v_cache (device) [num_pages][Hkv][page_size][D] (cache_dtype)

@@ -111,11 +111,10 @@ def test_plan_and_workspace_host_logic(L):
         1 * 1 * 72 * 64 * 130 * 4
     # one partition of a decode shape: no workspace
     assert fp8kv.fp8kv_paged_attention_workspace_size(1, 1, 72, 8, 128, 64, 4096, -1, 4096) == 0
-    # verifier rows (12 x 9 = 108 per KV head): the E4M3 split of Q (two 128-byte
-    # rows and a multiplier per query row), even with one partition
-    rows = 1 * 12 * 72
-    assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 4096) == \
-        -(-(rows * 260) // 256) * 256
+    # verifier rows in one partition: no workspace either; in two, the partials
+    assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 4096) == 0
+    assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 2048) == \
+        1 * 12 * 72 * 2 * 130 * 4
     # a window of 512 with 12 rows spans at most ceil(523/64)+1 = 10 pages of 64
     ns, st = fp8kv.fp8kv_paged_attention_plan(1, 12, 72, 8, 128, 64, 8192, 511, 64)
     assert ns == 10

@@ -141,6 +141,29 @@ def test_verifier_rows_run_on_the_tensor_memory_kernel():
         assert_close(out, ref, f"split={st}")
 
 
+@pytest.mark.parametrize("L,window,split,msl,cluster", [
+    (1000, None, 128, None, 8), (1000, None, 256, None, 4), (600, 200, 128, None, 2), (4096, None, 512, None, 8),
+    (300, None, 128, None, 3), (500, None, 128, 1000, 8), (2000, None, 128, None, 1)])
+def test_single_sequence_cluster_combine(L, window, split, msl, cluster):
+    """One sequence in 2..8 partitions: the partitions of a KV head run as one
+    thread-block cluster and combine in distributed shared memory (no reduce
+    kernel); a larger max_seq_len leaves cluster CTAs without keys; more than
+    8 partitions take the workspace partials and the reduce kernel."""
+    case = gen.layer_case(9100 + L + split, [L], 12, 32, window=window)
+    if msl is not None:      # room in the block table for max_seq_len (the extra entries are never read)
+        bt = case.layout.block_table
+        extra = -(-msl // 32) - bt.shape[1]
+        case.layout.block_table = torch.cat([bt, torch.full((bt.shape[0], extra), -1, dtype=bt.dtype)], 1)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    ref = oracle_attention(case, okc, ovc)
+    out = gpu_attention(case, kc, vc, ks, vs, split_tokens=split, max_seq_len=msl)
+    d = fp8kv().fp8kv_last_dispatch()
+    assert d.startswith("attention_tc") and f"cluster={cluster} " in d, d
+    assert ("reduce=1" in d) == (cluster == 1), d
+    assert_close(out, ref, f"L={L} split={split}")
+
+
 @pytest.mark.parametrize("M,G", [(2, 9), (2, 16), (6, 9), (8, 16), (12, 10), (16, 8), (3, 11)])
 def test_tensor_memory_kernel_row_counts(M, G):
     """Row counts 18..128 through the tcgen05 kernel, both page sizes."""

@@ -656,6 +656,12 @@ static int check_sizes(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq
     return FP8KV_OK;
 }
 
+// Rows per KV head served by the tcgen05 kernel (on an E4M3 cache).
+static bool tc_rows(int M, int Hq, int Hkv) {
+    const int R = M * (Hq / Hkv);
+    return R > 16 && R <= 128;
+}
+
 static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_len, int window_left,
                      int split_tokens, Plan* p) {
     int rc = check_sizes(B, M, Hq, Hkv, D, PS, max_seq_len, window_left, split_tokens);
@@ -679,6 +685,11 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
         // sequence keep the longest ones from holding an SM alone at the end
         // of the launch (sequence lengths are only known on the device)
         if (ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
+        // one sequence of verifier rows spanning at most 8 tiles of 128 keys:
+        // a tile per partition (the partitions of a KV head then run as one
+        // thread-block cluster and combine on chip)
+        if (B == 1 && tc_rows(M, Hq, Hkv) && ceil_div(pages * PS, tc_tile_tokens()) <= 8)
+            sp = max(1, tc_tile_tokens() / PS);
     }
     sp = max(1, min(sp, pages));
     // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
@@ -692,23 +703,12 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
     return FP8KV_OK;
 }
 
-// Workspace: [Q split for the tcgen05 kernel][partial O][partial (m, l)].
-// The Q split (E4M3 hi and lo rows and a per-row logit multiplier) is
-// reserved for every shape the tcgen05 kernel may take (16 < M*G <= 128).
-static bool tc_rows(int M, int Hq, int Hkv) {
-    const int R = M * (Hq / Hkv);
-    return R > 16 && R <= 128;
-}
-static size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
-static size_t qsplit_bytes(int B, int M, int Hq, int Hkv) {
-    if (!tc_rows(M, Hq, Hkv)) return 0;
-    const size_t rows = (size_t)B * M * Hq;
-    return align256(rows * 128 * 2 + rows * 4);
-}
+// Workspace: [partial O][partial (m, l)] when a sequence spans several
+// partitions (reserved even when the partitions combine on chip).
 static size_t ws_bytes(int B, int M, int Hq, int Hkv, const Plan& p) {
-    size_t n = qsplit_bytes(B, M, Hq, Hkv);
-    if (p.num_splits > 1) n += (size_t)B * M * Hq * p.num_splits * (128 + 2) * sizeof(float);
-    return n;
+    (void)Hkv;
+    if (p.num_splits <= 1) return 0;
+    return (size_t)B * M * Hq * p.num_splits * (128 + 2) * sizeof(float);
 }
 
 // Opt in to the kernel's dynamic shared memory once per device (so that calls
@@ -790,19 +790,14 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
         !make_cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
         return FP8KV_ERR_CUDA;
 
-    AttnParams P;
+    AttnParams P = {};
     P.q = (const uint16_t*)q;
     P.block_table = block_table;
     P.seq_lens = seq_lens;
     P.k_scale = k_scale;
     P.v_scale = v_scale;
-    const size_t qb = qsplit_bytes(B, M, Hq, Hkv);
     const size_t rows = (size_t)B * M * Hq;
-    uint8_t* ws = (uint8_t*)workspace;
-    P.q_hi = qb ? ws : nullptr;
-    P.q_lo = qb ? ws + rows * 128 : nullptr;
-    P.q_mult = qb ? (float*)(ws + rows * 256) : nullptr;
-    P.ws_o = plan.num_splits > 1 ? (float*)(ws + qb) : nullptr;
+    P.ws_o = plan.num_splits > 1 ? (float*)workspace : nullptr;
     P.ws_ml = plan.num_splits > 1 ? P.ws_o + rows * plan.num_splits * 128 : nullptr;
     P.out = (uint16_t*)out;
     P.sm_scale = sm_scale;
@@ -842,6 +837,9 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     // up to 128 query rows per KV head on E4M3 pages, partitions of whole
     // 128-key tiles: tcgen05 kernel (one 128-row MMA tile); otherwise mma.sync
     const bool use_tc = fp8 && tc_rows(M, Hq, Hkv) && (plan.split_tokens % tc_tile_tokens()) == 0;
+    // one sequence in at most 8 partitions: the partitions of a KV head run
+    // as one thread-block cluster and combine in distributed shared memory
+    P.cluster = (use_tc && B == 1 && plan.num_splits > 1 && plan.num_splits <= 8) ? plan.num_splits : 0;
     if (use_tc)
         rc = launch_attention_tc(tk, tv, P, s);
     else if (page_size == 32)
@@ -849,7 +847,7 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     else
         rc = fp8 ? launch<64, true>(tk, tv, P, s) : launch<64, false>(tk, tv, P, s);
     if (rc) return rc;
-    if (plan.num_splits > 1) {
+    if (plan.num_splits > 1 && P.cluster <= 1) {
         const int64_t warps = (int64_t)B * M * Hq;
         cudaError_t e = launch_pdl(attn_reduce_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
                                    (const float*)P.ws_o, (const float*)P.ws_ml, seq_lens, B, M, Hq,
@@ -864,9 +862,9 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     if (use_tc)
         snprintf(buf, sizeof buf,
                  "attention_tc<ps=%d,e4m3> rows=%d tile=128x128 splits=%d split_tokens=%d grid=%dx%dx%d threads=%d "
-                 "reduce=%d",
+                 "cluster=%d reduce=%d",
                  page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B, tc_threads(),
-                 plan.num_splits > 1 ? 1 : 0);
+                 P.cluster > 1 ? P.cluster : 1, (plan.num_splits > 1 && P.cluster <= 1) ? 1 : 0);
     else
         snprintf(buf, sizeof buf,
                  "%s<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "

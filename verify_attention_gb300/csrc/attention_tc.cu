@@ -8,11 +8,11 @@
 //
 // Q.K^T runs natively in FP8: the E4M3 K tile is the B operand straight from
 // the TMA staging buffer (its 128-byte rows with the 128-byte swizzle are the
-// K-major operand layout), and each Q row is split by a pre-pass kernel into
-// two E4M3 terms after a per-row power-of-two scale, q' = q * 2^sh = Q_hi +
-// Q_lo, which is exact for every bf16 element within 2^-10 of the row maximum
-// (the rest is off by at most 2^-17 of the row maximum); the softmax warps
-// store both rows into tensor memory (A operand) and two accumulating MMAs
+// K-major operand layout), and each Q row is split in the kernel into two
+// E4M3 terms after a per-row power-of-two scale, q' = q * 2^sh = Q_hi + Q_lo,
+// which is exact for every bf16 element within 2^-10 of the row maximum (the
+// rest is off by at most 2^-17 of the row maximum); the softmax warps store
+// both into tensor memory (A operand) and two accumulating MMAs
 // give S = q'.K.  P.V runs in f16: P (softmax weights) is written to tensor
 // memory and is the A operand, V is widened E4M3 -> f16 (exact) into a
 // swizzled MN-major tile.  Rows past M x G (up to 128) carry Q = 0.
@@ -120,39 +120,6 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// Q split pre-pass, one warp per query row (lane l: dims 4l..4l+3):
-// q' = q * 2^sh with the row maximum |q'| in [128, 256), Q_hi = e4m3(q'),
-// Q_lo = e4m3(q' - Q_hi), and the row's logit multiplier
-// k_scale * sm_scale * log2(e) * 2^-sh.
-__global__ void __launch_bounds__(256) q_split_kernel(const uint2* __restrict__ q, int64_t rows,
-                                                      const float* __restrict__ k_scale, float sm_scale,
-                                                      uint32_t* __restrict__ q_hi, uint32_t* __restrict__ q_lo,
-                                                      float* __restrict__ q_mult) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (row >= rows) return;
-    const uint2 w = q[row * 32 + lane];
-    const float x0 = bf16_lo(w.x), x1 = bf16_hi(w.x), x2 = bf16_lo(w.y), x3 = bf16_hi(w.y);
-    float amax = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    int e = 7;
-    const uint32_t ab = __float_as_uint(amax);
-    if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
-        const int be = (int)((ab >> 23) & 0xff);
-        e = be ? be - 127 : -127;
-    }
-    const int sh = max(-100, min(100, 7 - e));
-    const float scale = ldexpf(1.0f, sh);
-    uint32_t hi, lo;
-    e4m3_split4(x0 * scale, x1 * scale, x2 * scale, x3 * scale, hi, lo);
-    q_hi[row * 32 + lane] = hi;
-    q_lo[row * 32 + lane] = lo;
-    if (lane == 0) q_mult[row] = (*k_scale) * sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
-}
-
 template <int PS>
 __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
@@ -209,11 +176,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
 
     pdl_wait();
     const int L = P.seq_lens[b];
-    bool run = true;                                        // uniform over the CTA
-    if (L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps) {
-        if (threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
-        run = false;
-    }
+    const bool seq_ok = !(L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps);
+    bool run = seq_ok;                                      // uniform over the CTA
+    if (!seq_ok && threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
     const int lo0 = (P.window_left >= 0) ? max(0, L - P.M - P.window_left) : 0;
     const int first_page = lo0 / PS, last_page = (L - 1) / PS;
     const int nsplit_b = (last_page - first_page + P.split_pages) / P.split_pages;
@@ -382,24 +347,62 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int p_r = L - P.M + m;
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
         const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
-        const float mult = P.q_mult[row_idx];
         const float vs = *P.v_scale;
         // rows past M*G get Q = 0: their (unused) weights stay finite and their
         // lanes take the same unmasked path as the real rows
         const bool pad = r >= P.R;
+        float mult;
         {
-            // the pre-split Q row: half 0 stores Q_hi, half 1 Q_lo (A operand of Q.K^T)
-            const uint4* src = (const uint4*)((half == 0 ? P.q_hi : P.q_lo) + row_idx * 128);
-            uint32_t qw[32];
+            // Q row split in place: q' = q * 2^sh with the row maximum |q'| in
+            // [128, 256) (from all 128 dims), Q_hi = e4m3(q'), Q_lo =
+            // e4m3(q' - Q_hi); this half stores dims 64*half .. +63 of both
+            // into tensor memory (the A operand of Q.K^T).  q' is exact in f16
+            // (8 significant bits, at most 256) and so is q' - Q_hi.
+            const uint4* src = (const uint4*)(P.q + row_idx * 128) + 8 * half;
+            uint32_t qh[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const uint4 w = pad ? make_uint4(0, 0, 0, 0) : src[u];
-                qw[4 * u] = w.x;
-                qw[4 * u + 1] = w.y;
-                qw[4 * u + 2] = w.z;
-                qw[4 * u + 3] = w.w;
+                qh[4 * u] = w.x;
+                qh[4 * u + 1] = w.y;
+                qh[4 * u + 2] = w.z;
+                qh[4 * u + 3] = w.w;
             }
-            tmem_st_x32(lane_base + (half == 0 ? TM_QH : TM_QL), qw);
+            // row maximum: this half's 64 dims, then the partner warp's through
+            // shared memory (named barrier of the quarter's two warps)
+            uint32_t am = 0;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) am = max_bf16x2(am, qh[u] & 0x7fff7fffu);
+            float amax = fmaxf(bf16_lo(am), bf16_hi(am));
+            xch[half * 128 + r] = amax;
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");
+            amax = fmaxf(xch[r], xch[128 + r]);
+            asm volatile("bar.sync %0, 64;" ::"r"(1 + wq) : "memory");   // xch free for the tile loop
+            int e = 7;
+            const uint32_t ab = __float_as_uint(amax);
+            if (amax > 0.f && ((ab >> 23) & 0xff) != 0xff) {
+                const int be = (int)((ab >> 23) & 0xff);
+                e = be ? be - 127 : -127;
+            }
+            const int sh = max(-100, min(100, 7 - e));
+            const float scale = ldexpf(1.0f, sh);
+            mult = (*P.k_scale) * P.sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+            uint32_t hw[16], lw[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                uint32_t h2[2], l2[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const uint32_t x = qh[2 * k + i];
+                    const uint32_t q16 = pack_f16x2(bf16_lo(x) * scale, bf16_hi(x) * scale);
+                    h2[i] = f16x2_to_e4m3x2(q16);
+                    l2[i] = f16x2_to_e4m3x2(sub_f16x2(q16, e4m3x2_to_f16x2(h2[i])));
+                }
+                hw[k] = h2[0] | (h2[1] << 16);
+                lw[k] = l2[0] | (l2[1] << 16);
+            }
+            tmem_st_x16(lane_base + TM_QH + 16 * half, hw);
+            tmem_st_x16(lane_base + TM_QL + 16 * half, lw);
             tmem_wait_st();
         }
         fence_before();
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         if (ok && active) {
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const bool direct = nsplit_b == 1;
+            const bool combine = !direct && P.cluster > 1;  // partial stays in shared memory
             const float f = direct ? vs / l_tot : vs;
             // This thread's half row (64 dims: bf16 output or fp32 partial)
             // goes through the free staging buffers to one bulk copy: stores
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                                               __uint_as_float(ov[4 * v4 + 2]) * f, __uint_as_float(ov[4 * v4 + 3]) * f);
                 }
             }
-            if (r < P.R) {
+            if (r < P.R && !combine) {
                 fence_proxy_async();        // the staged row, written by this thread, to the bulk copy
                 if (direct)
                     bulk_store(P.out + row_idx * 128 + 64 * half, smem_u32(row_stage), 128);
@@ -541,10 +545,65 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 bulk_wait_read();
             }
             if (r < P.R && !direct && half == 0) {
-                P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
-                P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_tot;
+                if (combine) {
+                    xch[r] = m_run;                         // the tile exchange area is free now
+                    xch[128 + r] = l_tot;
+                } else {
+                    P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
+                    P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_tot;
+                }
             }
         }
+    }
+
+    if (P.cluster > 1) {
+        // ------------------------------------------------- cluster combine
+        // The partitions of this (KV head, sequence) are the CTAs of one
+        // cluster (rank = partition): each combines rows rank, rank + C, ...
+        // one warp per row, lane l owning dims 4l..4l+3, reading every
+        // partition's (m, l) and fp32 partial O from its shared memory:
+        // O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p.
+        __syncwarp();
+        cluster_sync_all();
+        if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
+            const int hh = lane >> 4;                       // staged half row of these dims
+            for (int r = split + P.cluster * warp; r < P.R; r += P.cluster * WARPS) {
+                // every remote load of the row first (one round trip), then the arithmetic
+                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 16;
+                float4 v[8];
+#pragma unroll
+                for (int p = 0; p < 8; ++p)
+                    v[p] = p < nsplit_b ? ld_dsmem_f32x4(dsmem_addr(src, p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                float mp = -INFINITY, lp = 0.f;
+                if (lane < nsplit_b) {
+                    mp = ld_dsmem_f32(dsmem_addr(&xch[r], lane));
+                    lp = ld_dsmem_f32(dsmem_addr(&xch[128 + r], lane));
+                }
+                float mstar = mp;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar);
+                float lsum = w * lp;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
+                    acc.x = fmaf(wp, v[p].x, acc.x);
+                    acc.y = fmaf(wp, v[p].y, acc.y);
+                    acc.z = fmaf(wp, v[p].z, acc.z);
+                    acc.w = fmaf(wp, v[p].w, acc.w);
+                }
+                const float inv = 1.0f / lsum;
+                const int m = r / P.G;
+                const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + r % P.G;
+                *(uint2*)(P.out + orow * 128 + 4 * lane) =
+                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();                                 // no CTA leaves while others read it
     }
 
     // ---------------------------------------------------------------- teardown
@@ -562,7 +621,7 @@ int tc_tile_tokens() { return tc::NK; }
 int tc_threads() { return tc::THREADS; }
 
 int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
-    if (P.R > 128 || P.R <= 16 || !P.q_hi) return FP8KV_ERR_UNSUPPORTED;
+    if (P.R > 128 || P.R <= 16) return FP8KV_ERR_UNSUPPORTED;
     if ((P.split_pages * P.page_size) % tc::NK) return FP8KV_ERR_UNSUPPORTED;
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
@@ -578,17 +637,11 @@ int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Attn
             done.insert({dev, kern});
         }
     }
-    const int64_t rows = (int64_t)P.B * P.M * P.Hq;
-    cudaError_t e = launch_pdl(tc::q_split_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, s,
-                               (const uint2*)P.q, rows, P.k_scale, P.sm_scale, (uint32_t*)P.q_hi,
-                               (uint32_t*)P.q_lo, P.q_mult);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return FP8KV_ERR_CUDA;
-    }
+    cudaError_t e;
     dim3 grid(P.num_splits, P.Hkv, P.B);
-    e = launch_pdl(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
-                   dim3(tc::THREADS), tc::SMEM, s, tk, tv, P);
+    if (P.cluster > 1 && (P.cluster > 8 || P.cluster != P.num_splits)) return FP8KV_ERR_UNSUPPORTED;
+    e = launch_pdl_cluster(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
+                           dim3(tc::THREADS), tc::SMEM, s, P.cluster, tk, tv, P);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 

@@ -49,19 +49,24 @@ __device__ __forceinline__ void e4m3x2_to_f32x2(uint32_t codes, float& lo, float
     hi = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
 }
 
-// Four fp32 values (already scaled so the row maximum lies in [128, 256))
-// -> their E4M3 leading terms x_hi = e4m3(x) and residual terms
-// x_lo = e4m3(x - x_hi), four codes per word (element 0 in bits 0..7).
-// x_hi + x_lo reproduces x exactly for every bf16 x of at least 2^-2
-// (residuals of at most four significant bits, all above the E4M3
-// subnormal step 2^-9); below that the pair is off by at most 2^-10.
-__device__ __forceinline__ void e4m3_split4(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
-    const uint32_t h01 = e4m3x2(x0, x1), h23 = e4m3x2(x2, x3);
-    float d0, d1, d2, d3;
-    e4m3x2_to_f32x2(h01, d0, d1);
-    e4m3x2_to_f32x2(h23, d2, d3);
-    hi = h01 | (h23 << 16);
-    lo = e4m3x2(x0 - d0, x1 - d1) | (e4m3x2(x2 - d2, x3 - d3) << 16);
+// f16x2 -> two E4M3 codes (bits 0..7 from the low half), round to nearest
+// even, saturating; no NaN sign fix-up (for operands, not stored bytes).
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -225,21 +230,59 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
 namespace fp8kv {
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream is finishing; it must call pdl_wait()
-// before reading anything that kernel may have written.
+// before reading anything that kernel may have written.  cluster_x > 1
+// groups that many consecutive CTAs along x into one thread-block cluster.
 template <typename... KArgs, typename... Args>
-static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                     cudaStream_t stream, Args&&... args) {
+static inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                             cudaStream_t stream, int cluster_x, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x > 1 ? cluster_x : 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+static inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                     cudaStream_t stream, Args&&... args) {
+    return launch_pdl_cluster(kernel, grid, block, smem, stream, 1, std::forward<Args>(args)...);
+}
+
+// ------------------------------------------------ thread-block clusters
+
+// The address of the same shared-memory object in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* p, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t a) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+// Every thread of every CTA of the cluster: writes before it are visible to
+// reads after it anywhere in the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 int launch_status();                    // FP8KV_OK or FP8KV_ERR_CUDA after a launch

@@ -33,7 +33,11 @@ __global__ void __launch_bounds__(256) insert_kernel(
     const int64_t row = i >> 4;                 // t * Hkv + h
     const int64_t t = row / Hkv;
     const int h = (int)(row - t * Hkv);
+    // every load is independent of the others: issue them all before the
+    // first use, one memory round trip instead of two
     const int64_t slot = slots[t];
+    const uint4 kx = k[i], vx = v[i];
+    const float ks = FP8 ? *k_scale : 1.f, vs = FP8 ? *v_scale : 1.f;
     if (slot < 0) return;
     if (slot >= num_slots) {
         if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
@@ -41,9 +45,7 @@ __global__ void __launch_bounds__(256) insert_kernel(
     }
     const int64_t page = slot / page_size, off = slot - page * page_size;
     const int64_t dst = ((page * Hkv + h) * page_size + off) * 128 + chunk * 8;  // element index
-    const uint4 kx = k[i], vx = v[i];
     if (FP8) {
-        const float ks = *k_scale, vs = *v_scale;
         uint2 ko, vo;
         ko.x = e4m3x2(__fdiv_rn(bf16_lo(kx.x), ks), __fdiv_rn(bf16_hi(kx.x), ks)) |
                (e4m3x2(__fdiv_rn(bf16_lo(kx.y), ks), __fdiv_rn(bf16_hi(kx.y), ks)) << 16);
