@@ -51,6 +51,42 @@ def peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+# DRAM traffic of the dominant kernel per launch, from an ncu capture kept in
+# profiles/: the summary names the kernel, the bytes and the SHA-256 of the
+# sources it was built from; a changed source makes the figure stale (None).
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "ncu_attention_tc_verify_global.md")
+KERNEL_SOURCES = ["verify_attention_gb300/csrc/attention_tc.cu", "verify_attention_gb300/csrc/attention.cuh",
+                  "verify_attention_gb300/csrc/common.cuh", "verify_attention_gb300/csrc/tcgen05_tmem.cuh"]
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(dispatch):
+    """(bytes per launch, note) for the tcgen05 verifier kernel, or (None, why)."""
+    if not dispatch.startswith("attention_tc"):
+        return None, "no capture for this kernel"
+    try:
+        fields = {}
+        for line in open(TRAFFIC_PROFILE):
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel_sources_sha256") != kernel_sources_sha256():
+            return None, "kernel changed since the capture"
+        if fields.get("dispatch", "").split(" cluster=")[0] != dispatch.split(" cluster=")[0]:
+            return None, "captured launch shape differs"
+        return int(fields["dram_bytes_per_launch"]), os.path.relpath(TRAFFIC_PROFILE, ROOT)
+    except (OSError, KeyError, ValueError):
+        return None, "no capture"
+
+
 # ------------------------------------------------------------- workloads
 
 class Layer:
@@ -537,6 +573,7 @@ def main():
 
     dom_bytes, dom_s, dom_flops, dispatch = dominant_kernel(w, stream)
     achieved = dom_bytes / dom_s / 1e9
+    traffic, traffic_note = measured_traffic(dispatch)
     e2e_s, h2d, d2h = e2e_measure(w, max(3, min(args.steps, 20)), stream)
 
     line = {
@@ -552,7 +589,7 @@ def main():
         "useful_flops_per_step": w.flops_per_step(),
         "gpu_launches": args.steps * sum(1 + 1 + (1 if l.ws_bytes else 0) for l in w.copies[0]),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": "fp8kv_paged_attention (partial + reduce) on the largest layer",
                      "launch_ms": dom_s * 1e3, "bytes_per_launch": dom_bytes,
                      "tflops": dom_flops / dom_s / 1e12, "dispatch": dispatch,

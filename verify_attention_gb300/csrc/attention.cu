@@ -685,11 +685,16 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
         // sequence keep the longest ones from holding an SM alone at the end
         // of the launch (sequence lengths are only known on the device)
         if (ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
-        // one sequence of verifier rows spanning at most 8 tiles of 128 keys:
-        // a tile per partition (the partitions of a KV head then run as one
-        // thread-block cluster and combine on chip)
-        if (B == 1 && tc_rows(M, Hq, Hkv) && ceil_div(pages * PS, tc_tile_tokens()) <= 8)
-            sp = max(1, tc_tile_tokens() / PS);
+        // one sequence of verifier rows (one CTA per SM): at most 8 tiles of
+        // 128 keys get a tile per partition (the partitions of a KV head then
+        // run as one thread-block cluster and combine on chip); longer ones
+        // one wave of partitions over the SMs, whole tiles each
+        if (B == 1 && tc_rows(M, Hq, Hkv)) {
+            const int tile_pages = max(1, tc_tile_tokens() / PS);
+            const int tiles = ceil_div(pages, tile_pages);
+            const int wave = max(1, num_sms() / Hkv);
+            sp = tiles <= 8 ? tile_pages : tile_pages * ceil_div(tiles, min(tiles, wave));
+        }
     }
     sp = max(1, min(sp, pages));
     // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
