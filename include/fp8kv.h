@@ -87,7 +87,8 @@ typedef enum {
  *   slot_mapping  (device) int64 [T]
  *   k_scale, v_scale (device) one fp32 each, > 0 (E4M3 only)
  *   k_cache, v_cache (device) [num_pages][Hkv][page_size][D] of the cache dtype
- *   D must be 128; page_size 32 or 64; T may be 0 (no launch).
+ *   D must be 128; page_size 32 or 64; T may be 0 (no launch, FP8KV_OK, no
+ *   pointer is read).
  * Device check: slot >= num_pages*page_size -> row skipped, FP8KV_DEV_BAD_SLOT.
  */
 int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping, int T,
@@ -120,6 +121,7 @@ int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping
  *   other arguments as fp8kv_cache_insert.
  * Device checks: position outside [0, max_pos) -> token skipped entirely
  * (FP8KV_DEV_BAD_POSITION); bad slot -> K/V of that token skipped.
+ * T = 0 launches nothing and returns FP8KV_OK without reading any pointer.
  */
 int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const void* v,
                               const int64_t* positions, const void* q_norm_w,
@@ -185,7 +187,8 @@ size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D
  *                initialisation and are scratch after the call
  *   out          (device) bf16 [B][M][Hq][D]
  * Supported: D = 128, page_size 32 or 64, 1 <= M <= 16, Hq % Hkv == 0,
- * M * (Hq/Hkv) <= 144.  B = 0 launches nothing.
+ * M * (Hq/Hkv) <= 144.  B = 0 launches nothing and returns FP8KV_OK without
+ * reading any pointer.
  * Device checks: seq_len < M, seq_len > max_seq_len or more pages than
  * max_pages_per_seq -> that sequence's output is left untouched
  * (FP8KV_DEV_BAD_SEQ_LEN); page ids outside [0, num_pages) read zeros.

@@ -75,6 +75,9 @@ def test_attention_validation(L):
     assert _attn(L, ws=NULL) == E_WS
     assert _attn(L, wsb=16) == E_WS
     assert _attn(L, wl=-2) == E_INV
+    # B = 0: nothing to do, no pointer is read
+    assert _attn(L, B=0, q=NULL, k=NULL, v=NULL, bt=NULL, sl=NULL, out=NULL, ws=NULL, wsb=0) == 0
+    assert _attn(L, B=0, D=64) == E_UNS              # shapes are still checked
 
 
 def test_insert_validation(L):
@@ -91,6 +94,8 @@ def test_insert_validation(L):
     bad = list(args); bad[6] = NULL
     assert f(*bad) == 1
     bad = list(args); bad[3] = 0                    # T = 0: nothing to do
+    assert f(*bad) == 0
+    bad = [NULL, NULL, NULL, 0, 8, 128, NULL, NULL, NULL, NULL, 16, 32, 0, NULL]   # and no pointer is read
     assert f(*bad) == 0
     g = L.fp8kv_qk_norm_rope_insert
     a2 = [P16, P16, P16, P16, P16, P16, 1e-6, P16, 100, ctypes.c_void_p(2 << 20), P16, 4, 72, 8, 128, P16,

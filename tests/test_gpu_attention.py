@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from verify_attention_gb300 import build, inputs as gen
 from tests.helpers import (assert_close, gpu_attention, gpu_caches, oracle_attention, oracle_caches,
                            sample_rows)
@@ -198,6 +199,53 @@ def test_decode_kernel_key_groups(ps, dtype):
         out = gpu_attention(case, kc, vc, ks, vs, split_tokens=st)
         assert fp8kv().fp8kv_last_dispatch().startswith("paged_decode_mma")
         assert_close(out, ref, f"ps={ps} {dtype} split={st}")
+
+
+@pytest.mark.parametrize("M,ps", [(1, 32), (12, 32), (12, 64)])
+def test_window_of_one_key_returns_own_value(M, ps):
+    """window_left = 0: every row sees only its own key, so the output is that
+    key's dequantized V row (up to the bf16 output rounding), on every kernel."""
+    case = gen.layer_case(9300 + M + ps, [700, 130], M, ps, window=1)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    ref = oracle_attention(case, okc, ovc, window_left=0)
+    for st in (0, ps, 4 * ps):
+        out = gpu_attention(case, kc, vc, ks, vs, split_tokens=st, window_left=0)
+        assert_close(out, ref, f"M={M} ps={ps} split={st}")
+    # the closed form: V of position L - M + m, from the cache bytes
+    lay = case.layout
+    for b in range(2):
+        L = int(lay.seq_lens[b])
+        for m in range(M):
+            pos = L - M + m
+            page = int(lay.block_table[b, pos // ps])
+            want = oracle.e4m3_decode(ovc[page, :, pos % ps, :]) * case.v_scale   # [Hkv][128]
+            got = out[b, m].float().cpu().numpy().reshape(8, 9, 128)
+            np.testing.assert_allclose(got, np.repeat(want[:, None, :], 9, 1), rtol=1e-2, atol=1e-6)
+
+
+@pytest.mark.parametrize("M,G", [(2, 8), (1, 16)])
+def test_sixteen_rows_fill_one_decode_tile(M, G):
+    """Exactly 16 rows per KV head: the decode kernel with a full row tile."""
+    case = gen.layer_case(9400 + M * G, [333, 64], M, 32, Hq=2 * G, Hkv=2)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    out = gpu_attention(case, kc, vc, ks, vs)
+    assert fp8kv().fp8kv_last_dispatch().startswith("paged_decode_mma")
+    assert_close(out, oracle_attention(case, okc, ovc), f"M={M} G={G}")
+
+
+def test_empty_batch_launches_nothing():
+    """B = 0: the call succeeds and leaves the output untouched."""
+    from verify_attention_gb300 import fp8kv as f
+    q = torch.zeros(0, 12, 72, 128, dtype=torch.bfloat16, device="cuda")
+    cache = torch.zeros(4, 8, 32, 128, dtype=torch.uint8, device="cuda")
+    bt = torch.zeros(0, 4, dtype=torch.int32, device="cuda")
+    sl = torch.zeros(0, dtype=torch.int32, device="cuda")
+    s = torch.ones(1, device="cuda")
+    out = f.fp8kv_paged_attention(q, cache, cache, bt, sl, 128, s, s, 0.088)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 12, 72, 128)
 
 
 # ------------------------------------------------------------ the configs

@@ -779,6 +779,7 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     Plan plan;
     int rc = make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &plan);
     if (rc) return rc;
+    if (B == 0) return FP8KV_OK;                                // nothing to do; no pointer is read
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
     if (fp8 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID_ARG;
     if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(out)) return FP8KV_ERR_INVALID_ARG;
@@ -788,7 +789,6 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     if (!(sm_scale == sm_scale)) return FP8KV_ERR_INVALID_ARG;
     const size_t need = ws_bytes(B, M, Hq, Hkv, plan);
     if (need && (!workspace || workspace_bytes < need || !al16(workspace))) return FP8KV_ERR_WORKSPACE;
-    if (B == 0) return FP8KV_OK;
 
     CUtensorMap tk, tv;
     if (!make_cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||

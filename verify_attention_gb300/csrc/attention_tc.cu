@@ -507,7 +507,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const bool direct = nsplit_b == 1;
             const bool combine = !direct && P.cluster > 1;  // partial stays in shared memory
-            const float f = direct ? vs / l_tot : vs;
+            // direct: bf16 of O * v_scale / l; workspace partial: fp32 O * v_scale;
+            // cluster partial: f16 of O / l in code units (|x| <= 448, 11-bit
+            // mantissa), half the bytes the other CTAs pull
+            // (a row with no visible key in this partition has l = 0: weight 0, values 0)
+            const float f = direct ? vs / l_tot : (combine ? (l_tot > 0.f ? 1.0f / l_tot : 0.f) : vs);
             // This thread's half row (64 dims: bf16 output or fp32 partial)
             // goes through the free staging buffers to one bulk copy: stores
             // straight from the row-per-thread TMEM layout would touch a
@@ -527,6 +531,15 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
+                } else if (combine) {
+                    uint4* dst = (uint4*)(row_stage + c * 2);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        dst[v4] = make_uint4(
+                            pack_f16x2(__uint_as_float(ov[8 * v4 + 0]) * f, __uint_as_float(ov[8 * v4 + 1]) * f),
+                            pack_f16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
+                            pack_f16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
+                            pack_f16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
                 } else {
                     float4* dst = (float4*)(row_stage + c * 4);
 #pragma unroll
@@ -569,11 +582,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const int hh = lane >> 4;                       // staged half row of these dims
             for (int r = split + P.cluster * warp; r < P.R; r += P.cluster * WARPS) {
                 // every remote load of the row first (one round trip), then the arithmetic
-                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 16;
-                float4 v[8];
+                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 8;
+                uint2 v[8];
 #pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    v[p] = p < nsplit_b ? ld_dsmem_f32x4(dsmem_addr(src, p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int p = 0; p < 8; ++p) v[p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
                 float mp = -INFINITY, lp = 0.f;
                 if (lane < nsplit_b) {
                     mp = ld_dsmem_f32(dsmem_addr(&xch[r], lane));
@@ -582,20 +594,22 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 float mstar = mp;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar);
-                float lsum = w * lp;
+                // partition weight 2^(m_p - m*) l_p on its normalised partial
+                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar) * lp;
+                float lsum = w;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
                     const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
-                    acc.x = fmaf(wp, v[p].x, acc.x);
-                    acc.y = fmaf(wp, v[p].y, acc.y);
-                    acc.z = fmaf(wp, v[p].z, acc.z);
-                    acc.w = fmaf(wp, v[p].w, acc.w);
+                    const float2 a = f16x2_to_f32x2(v[p].x), c2 = f16x2_to_f32x2(v[p].y);
+                    acc.x = fmaf(wp, a.x, acc.x);
+                    acc.y = fmaf(wp, a.y, acc.y);
+                    acc.z = fmaf(wp, c2.x, acc.z);
+                    acc.w = fmaf(wp, c2.y, acc.w);
                 }
-                const float inv = 1.0f / lsum;
+                const float inv = *P.v_scale / lsum;
                 const int m = r / P.G;
                 const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + r % P.G;
                 *(uint2*)(P.out + orow * 128 + 4 * lane) =

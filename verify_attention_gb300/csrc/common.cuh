@@ -57,6 +57,11 @@ __device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h) {
     return r;
 }
 
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+    return make_float2(__half2float(__ushort_as_half((unsigned short)(h & 0xffffu))),
+                       __half2float(__ushort_as_half((unsigned short)(h >> 16))));
+}
+
 __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -271,12 +276,9 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
     return v;
 }
-__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t a) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(a)
-                 : "memory");
+__device__ __forceinline__ uint2 ld_dsmem_u32x2(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
     return v;
 }
 // Every thread of every CTA of the cluster: writes before it are visible to

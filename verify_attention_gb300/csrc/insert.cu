@@ -187,13 +187,13 @@ extern "C" int fp8kv_cache_insert(const void* k, const void* v, const int64_t* s
                                   int cache_dtype, void* stream) {
     if (T < 0 || Hkv <= 0 || num_pages <= 0) return FP8KV_ERR_INVALID_ARG;
     if (cache_dtype != FP8KV_CACHE_E4M3 && cache_dtype != FP8KV_CACHE_BF16) return FP8KV_ERR_INVALID_ARG;
+    if (D != 128) return FP8KV_ERR_UNSUPPORTED;
+    if (page_size != 32 && page_size != 64) return FP8KV_ERR_UNSUPPORTED;
+    if (T == 0) return FP8KV_OK;                                // nothing to do; no pointer is read
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return FP8KV_ERR_INVALID_ARG;
     if (cache_dtype == FP8KV_CACHE_E4M3 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID_ARG;
     if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
         return FP8KV_ERR_INVALID_ARG;
-    if (D != 128) return FP8KV_ERR_UNSUPPORTED;
-    if (page_size != 32 && page_size != 64) return FP8KV_ERR_UNSUPPORTED;
-    if (T == 0) return FP8KV_OK;
     const int64_t items = (int64_t)T * Hkv * 16;
     const int threads = 256;
     const int64_t blocks = (items + threads - 1) / threads;
@@ -215,17 +215,17 @@ extern "C" int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const voi
                                          const float* v_scale, void* k_cache, void* v_cache,
                                          int num_pages, int page_size, void* stream) {
     if (T < 0 || Hq <= 0 || Hkv <= 0 || num_pages <= 0 || max_pos <= 0) return FP8KV_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f)) return FP8KV_ERR_INVALID_ARG;
+    if (D != 128) return FP8KV_ERR_UNSUPPORTED;
+    if (page_size != 32 && page_size != 64) return FP8KV_ERR_UNSUPPORTED;
+    if (T == 0) return FP8KV_OK;                                // nothing to do; no pointer is read
     if (!q || !k || !v || !positions || !q_norm_w || !k_norm_w || !cos_sin || !q_out || !slot_mapping ||
         !k_scale || !v_scale || !k_cache || !v_cache)
         return FP8KV_ERR_INVALID_ARG;
-    if (!(eps >= 0.0f)) return FP8KV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(cos_sin) ||
         !aligned16(q_norm_w) || !aligned16(k_norm_w) || !aligned16(k_cache) || !aligned16(v_cache))
         return FP8KV_ERR_INVALID_ARG;
     if (q == q_out) return FP8KV_ERR_INVALID_ARG;
-    if (D != 128) return FP8KV_ERR_UNSUPPORTED;
-    if (page_size != 32 && page_size != 64) return FP8KV_ERR_UNSUPPORTED;
-    if (T == 0) return FP8KV_OK;
     const int64_t warps = (int64_t)T * (Hq + Hkv);
     const int64_t blocks = (warps + 7) / 8;
     if (blocks > 0x7fffffff) return FP8KV_ERR_UNSUPPORTED;
