@@ -5,9 +5,10 @@
 
 A step is one pass of the whole hot path over one batch:
   verify48   (default) 48 layers [SW512 x3, G] x12, B=1, M=12, L=8192: per
-             layer a 12-token E4M3 insert then paged attention (+ reduce);
+             layer a 12-token E4M3 insert then paged attention (+ reduce),
+             one fp8kv_append_paged_attention call;
   decode128k 12 global layers, B=1, M=1, L=131072, page 64: 1-token insert +
-             split-KV attention + reduce per layer;
+             split-KV attention + reduce per layer (one append call);
   serving64  8 layers G/SW512, B=64, L ~ U[1024, 32768], M=12, page 32:
              fused Q/K RMSNorm + RoPE + E4M3 insert, then attention.
 Inputs are seeded synthetic tensors generated on the device; the whole step
@@ -152,6 +153,22 @@ class Layer:
                                     self.vs, self.case.sm_scale, self.window_left, self.split_tokens,
                                     workspace=ws, out=self.out)
 
+    def step(self, ws):
+        """The layer's share of a step: the new tokens' insert, then attention.
+        Plain inserts of the new rows go through the one-call append entry
+        (same cache bytes and output as insert + attention); the fused
+        norm/RoPE boundary is its own call."""
+        from verify_attention_gb300 import fp8kv
+        if self.fused is None:
+            B, M, Hq, D = self.q.shape
+            fp8kv.fp8kv_append_paged_attention(self.k_new.view(B, M, -1, D), self.v_new.view(B, M, -1, D),
+                                               self.q, self.kc, self.vc, self.bt, self.sl, self.max_seq_len,
+                                               self.ks, self.vs, self.case.sm_scale, self.window_left,
+                                               self.split_tokens, workspace=ws, out=self.out)
+        else:
+            self.insert()
+            self.attend(ws)
+
     def attn_bytes(self):
         B, M, Hq, D = self.q.shape
         e = 1 if self.kc.dtype == torch.uint8 else 2
@@ -181,8 +198,7 @@ class Workload:
 
     def step(self, copy):
         for layer in self.copies[copy]:
-            layer.insert()
-            layer.attend(self.ws)
+            layer.step(self.ws)
 
     def bytes_per_step(self):
         return sum(l.attn_bytes() + l.insert_bytes() for l in self.copies[0])
@@ -363,7 +379,7 @@ def e2e_measure(w: Workload, steps, stream):
     host_in = []
     h2d = d2h = 0
     for l in layers:
-        srcs = [l.q, l.k_new, l.v_new, l.slots_new] if l.fused is None else [l.fq, l.fk, l.fv, l.fpos, l.fslots]
+        srcs = [l.q, l.k_new, l.v_new] if l.fused is None else [l.fq, l.fk, l.fv, l.fpos, l.fslots]
         hs = [t.cpu().pin_memory() for t in srcs]
         host_in.append((hs, srcs))
         h2d += sum(t.numel() * t.element_size() for t in hs)
@@ -376,8 +392,7 @@ def e2e_measure(w: Workload, steps, stream):
             for (hs, ds), l, ho in zip(host_in, layers, host_out):
                 for h, d in zip(hs, ds):
                     d.copy_(h, non_blocking=True)
-                l.insert()
-                l.attend(w.ws)
+                l.step(w.ws)
                 ho.copy_(l.out, non_blocking=True)
     one()
     torch.cuda.synchronize()

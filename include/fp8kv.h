@@ -202,6 +202,32 @@ int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cach
                           void* stream);
 
 /*
+ * fp8kv_append_paged_attention -- one verifier step of a layer: the M new
+ * tokens of every sequence are written to the cache, then attention runs
+ * ("calibrated FP8 KV on Intel B70", "Contract": the insert at the new rows'
+ * positions followed by the exact paged attention over the cache).
+ *
+ * Token m of sequence b (k_new, v_new: bf16 [B][M][Hkv][D], device) goes to
+ * position p = seq_lens[b] - M + m, i.e. slot
+ * block_table[b][p / page_size] * page_size + p % page_size, with the
+ * fp8kv_cache_insert encoding; then fp8kv_paged_attention runs with the same
+ * arguments.  Cache bytes and output are identical to fp8kv_cache_insert
+ * with those slots followed by fp8kv_paged_attention.  On the tensor-memory
+ * path the CTA whose partition holds a new position writes it before
+ * loading that page (no separate insert launch); otherwise an append kernel
+ * runs first.  k_new and v_new must be 16-byte aligned; B = 0 is a no-op.
+ * Device check: a block-table entry outside [0, num_pages) at a new
+ * position -> that token is not written (FP8KV_DEV_BAD_SLOT).
+ */
+int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const void* q, void* k_cache,
+                                 void* v_cache, int cache_dtype, const int32_t* block_table,
+                                 int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len, int B,
+                                 int M, int Hq, int Hkv, int D, int page_size, int num_pages,
+                                 const float* k_scale, const float* v_scale, float sm_scale,
+                                 int window_left, int split_tokens, void* workspace,
+                                 size_t workspace_bytes, void* out, void* stream);
+
+/*
  * fp8kv_paged_attention_noalloc -- fp8kv_paged_attention without a
  * caller-provided workspace.  (The pages have no counterpart: this is an
  * integration convenience, not part of the method.)

@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("fp8kv_cache_insert", "fp8kv_qk_norm_rope_insert", "fp8kv_paged_attention",
+              "fp8kv_append_paged_attention",
               "fp8kv_paged_attention_workspace_size", "fp8kv_paged_attention_plan",
               "fp8kv_status_string", "fp8kv_last_dispatch", "fp8kv_device_status"):
         assert n in names
@@ -78,6 +79,18 @@ def test_attention_validation(L):
     # B = 0: nothing to do, no pointer is read
     assert _attn(L, B=0, q=NULL, k=NULL, v=NULL, bt=NULL, sl=NULL, out=NULL, ws=NULL, wsb=0) == 0
     assert _attn(L, B=0, D=64) == E_UNS              # shapes are still checked
+
+
+def test_append_validation(L):
+    f = L.fp8kv_append_paged_attention
+    a = [P16, P16, P16, P16, P16, 0, P16, 4, P16, 100, 1, 12, 72, 8, 128, 32, 16, P16, P16, 0.088, -1, 32, P16,
+         1 << 30, P16, NULL]
+    bad = list(a); bad[0] = NULL                   # k_new missing
+    assert f(*bad) == 1
+    bad = list(a); bad[1] = ctypes.c_void_p((1 << 20) + 4)   # misaligned
+    assert f(*bad) == 1
+    bad = list(a); bad[10] = 0; bad[0] = NULL; bad[1] = NULL   # B = 0: nothing to do
+    assert f(*bad) == 0
 
 
 def test_insert_validation(L):

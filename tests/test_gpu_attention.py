@@ -248,6 +248,45 @@ def test_empty_batch_launches_nothing():
     assert out.shape == (0, 12, 72, 128)
 
 
+@pytest.mark.parametrize("seq_lens,M,ps,window,split", [
+    ([700], 12, 32, None, 0),            # one sequence: one wave of partitions + reduce
+    ([640], 12, 32, 512, 0),             # one sequence, sliding: cluster combine
+    ([1000], 12, 32, None, 128),         # 8-CTA cluster, new tokens straddling a tile edge
+    ([300, 1000, 77], 12, 64, None, 0),  # batch, tensor-memory kernel
+    ([130, 33], 12, 32, 40, 64),         # mma.sync kernel with the append kernel
+    ([500, 33], 1, 64, None, 0),         # decode kernel with the append kernel
+])
+def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split):
+    """fp8kv_append_paged_attention == fp8kv_cache_insert of the new rows at
+    their slots followed by fp8kv_paged_attention: identical cache bytes and
+    identical outputs, and within tolerance of the oracle."""
+    from verify_attention_gb300 import fp8kv as f
+    case = gen.layer_case(9500 + sum(seq_lens) + M + split, seq_lens, M, ps, window=window)
+    lay = case.layout
+    shape = (lay.num_pages, 8, ps, 128)
+    kc = torch.full(shape, 0xA5, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    ks = torch.tensor([case.k_scale], device="cuda")
+    vs = torch.tensor([case.v_scale], device="cuda")
+    if case.k_prior.shape[0]:
+        f.fp8kv_cache_insert(case.k_prior.cuda(), case.v_prior.cuda(), case.slots_prior.cuda(), ks, vs, kc, vc)
+    kc2, vc2 = kc.clone(), vc.clone()
+    f.fp8kv_cache_insert(case.k_new.cuda(), case.v_new.cuda(), case.slots_new.cuda(), ks, vs, kc2, vc2)
+    ref = gpu_attention(case, kc2, vc2, ks, vs, split_tokens=split)
+    B = len(seq_lens)
+    kn = case.k_new.cuda().view(B, M, 8, 128)
+    vn = case.v_new.cuda().view(B, M, 8, 128)
+    out = f.fp8kv_append_paged_attention(kn, vn, case.q.cuda(), kc, vc, lay.block_table.cuda(),
+                                         lay.seq_lens.cuda(), int(lay.seq_lens.max()), ks, vs, case.sm_scale,
+                                         window_left=case.window_left, split_tokens=split)
+    torch.cuda.synchronize()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(out, ref)
+    okc, ovc = oracle_caches(case)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert_close(out, oracle_attention(case, okc, ovc), f"append {seq_lens} M={M}")
+
+
 # ------------------------------------------------------------ the configs
 
 def test_cfg1_tiny_decode():

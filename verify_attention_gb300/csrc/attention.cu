@@ -768,12 +768,14 @@ extern "C" size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int
 
 static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cache, int cache_dtype,
-                                     const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
-                                     int max_seq_len, int B, int M, int Hq, int Hkv, int D, int page_size,
-                                     int num_pages, const float* k_scale, const float* v_scale, float sm_scale,
-                                     int window_left, int split_tokens, void* workspace, size_t workspace_bytes,
-                                     void* out, void* stream) {
+// The attention call; with k_new / v_new, the M new tokens of each sequence
+// are first written to the cache at positions L - M + m (append).
+static int attention_call(const void* k_new, const void* v_new, const void* q, const void* k_cache,
+                          const void* v_cache, int cache_dtype, const int32_t* block_table, int max_pages_per_seq,
+                          const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq, int Hkv, int D,
+                          int page_size, int num_pages, const float* k_scale, const float* v_scale, float sm_scale,
+                          int window_left, int split_tokens, void* workspace, size_t workspace_bytes, void* out,
+                          void* stream) {
     if (cache_dtype != FP8KV_CACHE_E4M3 && cache_dtype != FP8KV_CACHE_BF16) return FP8KV_ERR_INVALID_ARG;
     const bool fp8 = cache_dtype == FP8KV_CACHE_E4M3;
     Plan plan;
@@ -781,6 +783,8 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     if (rc) return rc;
     if (B == 0) return FP8KV_OK;                                // nothing to do; no pointer is read
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
+    if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!al16(k_new) || !al16(v_new))))
+        return FP8KV_ERR_INVALID_ARG;
     if (fp8 && (!k_scale || !v_scale)) return FP8KV_ERR_INVALID_ARG;
     if (!al16(q) || !al16(k_cache) || !al16(v_cache) || !al16(out)) return FP8KV_ERR_INVALID_ARG;
     if (num_pages <= 0 || max_pages_per_seq <= 0) return FP8KV_ERR_INVALID_ARG;
@@ -845,6 +849,17 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
     // one sequence in at most 8 partitions: the partitions of a KV head run
     // as one thread-block cluster and combine in distributed shared memory
     P.cluster = (use_tc && B == 1 && plan.num_splits > 1 && plan.num_splits <= 8) ? plan.num_splits : 0;
+    if (k_new && use_tc) {                                          // appended in the kernel
+        P.k_new = (const uint16_t*)k_new;
+        P.v_new = (const uint16_t*)v_new;
+        P.k_cache = (uint8_t*)k_cache;
+        P.v_cache = (uint8_t*)v_cache;
+        P.num_pages = num_pages;
+    } else if (k_new) {
+        rc = launch_append(k_new, v_new, seq_lens, block_table, max_pages_per_seq, B, M, Hkv, k_scale, v_scale,
+                           (void*)k_cache, (void*)v_cache, num_pages, page_size, fp8, s);
+        if (rc) return rc;
+    }
     if (use_tc)
         rc = launch_attention_tc(tk, tv, P, s);
     else if (page_size == 32)
@@ -879,6 +894,30 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
                  plan.num_splits, Hkv, B, (P.NT * P.KW + 1) * 32, plan.num_splits > 1 ? 1 : 0);
     set_dispatch(buf);
     return FP8KV_OK;
+}
+
+extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cache, int cache_dtype,
+                                     const int32_t* block_table, int max_pages_per_seq, const int32_t* seq_lens,
+                                     int max_seq_len, int B, int M, int Hq, int Hkv, int D, int page_size,
+                                     int num_pages, const float* k_scale, const float* v_scale, float sm_scale,
+                                     int window_left, int split_tokens, void* workspace, size_t workspace_bytes,
+                                     void* out, void* stream) {
+    return attention_call(nullptr, nullptr, q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq,
+                          seq_lens, max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, sm_scale,
+                          window_left, split_tokens, workspace, workspace_bytes, out, stream);
+}
+
+extern "C" int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const void* q, void* k_cache,
+                                            void* v_cache, int cache_dtype, const int32_t* block_table,
+                                            int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len, int B,
+                                            int M, int Hq, int Hkv, int D, int page_size, int num_pages,
+                                            const float* k_scale, const float* v_scale, float sm_scale,
+                                            int window_left, int split_tokens, void* workspace,
+                                            size_t workspace_bytes, void* out, void* stream) {
+    if (B > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
+    return attention_call(k_new, v_new, q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq, seq_lens,
+                          max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, sm_scale,
+                          window_left, split_tokens, workspace, workspace_bytes, out, stream);
 }
 
 // ================================================ allocation-free variant

@@ -23,7 +23,21 @@ struct AttnParams {
     // partial results through distributed shared memory, without workspace
     // partials or the reduce kernel
     int cluster;
+    // append (tcgen05 path): the M new tokens of each sequence, bf16
+    // [B][M][Hkv][128], are encoded into the cache at positions L - M + m by
+    // the CTA whose partition holds them before it loads those pages; null
+    // for a plain call
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint8_t* k_cache;
+    uint8_t* v_cache;
+    int num_pages;
 };
+
+// Append kernel (insert.cu): the same encoding for the other attention paths.
+int launch_append(const void* k, const void* v, const int32_t* seq_lens, const int32_t* block_table, int mpps, int B,
+                  int M, int Hkv, const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                  int num_pages, int page_size, bool fp8, cudaStream_t s);
 
 // Host launcher of the tcgen05 kernel (attention_tc.cu).  Returns
 // FP8KV_ERR_UNSUPPORTED when the shape is not one it implements.

@@ -73,7 +73,8 @@ enum {
     B_Q_READY = B_O_FINAL + 1,
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                    // one per TMEM lane quarter: the two softmax warps
-    B_COUNT = B_PAIR + 4
+    B_NEW = B_PAIR + 4,                         // append: the new tokens are in the cache
+    B_COUNT = B_NEW + 1
 };
 
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         mbar_init(bar(B_O_FINAL), 1);
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
+        mbar_init(bar(B_NEW), CONV_WARPS);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
@@ -192,6 +194,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     constexpr int PPT = NK / PS;                            // pages per tile
     const int n_tiles = (n_pages + PPT - 1) / PPT;
     const int k_begin = page_begin * PS;
+    // append: new tokens at positions [L - M, L) that fall in this partition
+    const int app_lo = max(L - P.M, k_begin), app_hi = min(L, k_begin + n_pages * PS);
+    const bool appends = P.k_new != nullptr && run && app_lo < app_hi;
     bool ok = true;
 
     if (!run) {
@@ -201,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const uint64_t policy = policy_evict_first();
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         int issued = 0;
+        bool new_seen = false;
         for (int base = 0; base < n_pages && ok; base += 32) {
             const int mine = (base + lane < n_pages) ? bt[base + lane] : 0;
             const int cnt = min(32, n_pages - base);
@@ -210,8 +216,14 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 const int t = i / PPT, pin = i % PPT;
                 const int s = t % STAGES, use = t / STAGES;
                 if (lane == 0) {
+                    // a page holding appended tokens is loaded once they are written
+                    const int pk = (page_begin + i) * PS;
+                    if (appends && pk < app_hi && pk + PS > app_lo && !new_seen) {
+                        ok = mbar_wait(bar(B_NEW), 0);
+                        new_seen = true;
+                    }
                     if (pin == 0) {
-                        if (use > 0) ok = mbar_wait(bar(B_STG_EMPTY + s), (use - 1) & 1);
+                        if (use > 0 && ok) ok = mbar_wait(bar(B_STG_EMPTY + s), (use - 1) & 1);
                         const int pages_here = min(PPT, n_pages - t * PPT);
                         if (ok) mbar_expect_tx(bar(B_STG_FULL + s), pages_here * PS * 128 * 2);
                     }
@@ -283,6 +295,30 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // Keys outside every row's range are written as zeros, so stale or NaN
         // bytes there cannot reach the output.
         const int ct = converter_index(warp) * 32 + lane;
+        if (appends) {
+            // ---------------------------------------------- append insert
+            // the converter warps encode this head's appended tokens (the
+            // cache-insert encoding, one 8-element chunk of K and of V per
+            // item) into the cache, then let the producer load those pages
+            const int n = app_hi - app_lo;
+            const float ksc = *P.k_scale, vsc = *P.v_scale;
+            for (int it = ct; it < n * 16; it += CONV_THREADS) {
+                const int pos = app_lo + (it >> 4), chunk = it & 15, m = pos - (L - P.M);
+                const int64_t src = (((int64_t)b * P.M + m) * P.Hkv + hk) * 16 + chunk;
+                const uint4 kx = ((const uint4*)P.k_new)[src], vx = ((const uint4*)P.v_new)[src];
+                const int page = P.block_table[(int64_t)b * P.mpps + pos / PS];
+                if (page < 0 || page >= P.num_pages) {
+                    if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
+                    continue;
+                }
+                const int64_t dst = (((int64_t)page * P.Hkv + hk) * PS + pos % PS) * 128 + chunk * 8;
+                *(uint2*)(P.k_cache + dst) = e4m3_encode8(kx, ksc);
+                *(uint2*)(P.v_cache + dst) = e4m3_encode8(vx, vsc);
+            }
+            asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes before the TMA reads
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_NEW));
+        }
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % STAGES, vb = t % VBUFS;
             ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);

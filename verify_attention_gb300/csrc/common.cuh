@@ -89,6 +89,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// Eight bf16 values (one 16-byte chunk) -> eight E4M3 codes of x / scale,
+// each with one fp32 IEEE division (the cache-insert encoding).
+__device__ __forceinline__ uint2 e4m3_encode8(uint4 x, float scale) {
+    uint2 o;
+    o.x = e4m3x2(__fdiv_rn(bf16_lo(x.x), scale), __fdiv_rn(bf16_hi(x.x), scale)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(x.y), scale), __fdiv_rn(bf16_hi(x.y), scale)) << 16);
+    o.y = e4m3x2(__fdiv_rn(bf16_lo(x.z), scale), __fdiv_rn(bf16_hi(x.z), scale)) |
+          (e4m3x2(__fdiv_rn(bf16_lo(x.w), scale), __fdiv_rn(bf16_hi(x.w), scale)) << 16);
+    return o;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

@@ -10,6 +10,7 @@
 //
 // Both kernels are HBM-bound streaming kernels: every thread moves 16 B of
 // bf16 in and 8 B of codes out with one vector load and one vector store.
+#include "attention.cuh"
 #include "common.cuh"
 
 namespace fp8kv {
@@ -46,21 +47,67 @@ __global__ void __launch_bounds__(256) insert_kernel(
     const int64_t page = slot / page_size, off = slot - page * page_size;
     const int64_t dst = ((page * Hkv + h) * page_size + off) * 128 + chunk * 8;  // element index
     if (FP8) {
-        uint2 ko, vo;
-        ko.x = e4m3x2(__fdiv_rn(bf16_lo(kx.x), ks), __fdiv_rn(bf16_hi(kx.x), ks)) |
-               (e4m3x2(__fdiv_rn(bf16_lo(kx.y), ks), __fdiv_rn(bf16_hi(kx.y), ks)) << 16);
-        ko.y = e4m3x2(__fdiv_rn(bf16_lo(kx.z), ks), __fdiv_rn(bf16_hi(kx.z), ks)) |
-               (e4m3x2(__fdiv_rn(bf16_lo(kx.w), ks), __fdiv_rn(bf16_hi(kx.w), ks)) << 16);
-        vo.x = e4m3x2(__fdiv_rn(bf16_lo(vx.x), vs), __fdiv_rn(bf16_hi(vx.x), vs)) |
-               (e4m3x2(__fdiv_rn(bf16_lo(vx.y), vs), __fdiv_rn(bf16_hi(vx.y), vs)) << 16);
-        vo.y = e4m3x2(__fdiv_rn(bf16_lo(vx.z), vs), __fdiv_rn(bf16_hi(vx.z), vs)) |
-               (e4m3x2(__fdiv_rn(bf16_lo(vx.w), vs), __fdiv_rn(bf16_hi(vx.w), vs)) << 16);
-        *reinterpret_cast<uint2*>(k_cache + dst) = ko;
-        *reinterpret_cast<uint2*>(v_cache + dst) = vo;
+        *reinterpret_cast<uint2*>(k_cache + dst) = e4m3_encode8(kx, ks);
+        *reinterpret_cast<uint2*>(v_cache + dst) = e4m3_encode8(vx, vs);
     } else {
         *reinterpret_cast<uint4*>(k_cache + dst * 2) = kx;
         *reinterpret_cast<uint4*>(v_cache + dst * 2) = vx;
     }
+}
+
+// ---------------------------------------------------------- append insert
+
+// The M new tokens of every sequence to positions L_b - M + m, through the
+// block table (the slots an insert of the verifier's new rows would name).
+// One thread per (sequence, row, head, 8-element chunk).
+template <bool FP8>
+__global__ void __launch_bounds__(256) append_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ block_table, int mpps, int B, int M, int Hkv, const float* __restrict__ k_scale,
+    const float* __restrict__ v_scale, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+    int num_pages, int page_size) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)B * M * Hkv * 16) return;
+    const int chunk = (int)(i & 15);
+    const int64_t row = i >> 4;                 // (b * M + m) * Hkv + h
+    const int h = (int)(row % Hkv);
+    const int64_t bm = row / Hkv;
+    const int b = (int)(bm / M), m = (int)(bm % M);
+    const int L = seq_lens[b];
+    const uint4 kx = k[i], vx = v[i];
+    const float ks = FP8 ? *k_scale : 1.f, vs = FP8 ? *v_scale : 1.f;
+    const int pos = L - M + m;
+    if (L < M || (L + page_size - 1) / page_size > mpps) {
+        if (chunk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+        return;
+    }
+    const int page = block_table[(int64_t)b * mpps + pos / page_size];
+    if (page < 0 || page >= num_pages) {
+        if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
+        return;
+    }
+    const int64_t dst = (((int64_t)page * Hkv + h) * page_size + pos % page_size) * 128 + chunk * 8;
+    if (FP8) {
+        *reinterpret_cast<uint2*>(k_cache + dst) = e4m3_encode8(kx, ks);
+        *reinterpret_cast<uint2*>(v_cache + dst) = e4m3_encode8(vx, vs);
+    } else {
+        *reinterpret_cast<uint4*>(k_cache + dst * 2) = kx;
+        *reinterpret_cast<uint4*>(v_cache + dst * 2) = vx;
+    }
+}
+
+int launch_append(const void* k, const void* v, const int32_t* seq_lens, const int32_t* block_table, int mpps, int B,
+                  int M, int Hkv, const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                  int num_pages, int page_size, bool fp8, cudaStream_t s) {
+    const int64_t items = (int64_t)B * M * Hkv * 16;
+    const int64_t blocks = (items + 255) / 256;
+    if (blocks > 0x7fffffff) return FP8KV_ERR_UNSUPPORTED;
+    cudaError_t e = launch_pdl(fp8 ? append_kernel<true> : append_kernel<false>, dim3((unsigned)blocks), dim3(256), 0,
+                               s, (const uint4*)k, (const uint4*)v, seq_lens, block_table, mpps, B, M, Hkv, k_scale,
+                               v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache, num_pages, page_size);
+    return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
 // ------------------------------------------------ fused RMSNorm+RoPE+insert

@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_paged_attention.restype = i32
         L.fp8kv_paged_attention.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32, i32,
                                             i32, i32, vp, vp, f32, i32, i32, vp, sz, vp, vp]
+        L.fp8kv_append_paged_attention.restype = i32
+        L.fp8kv_append_paged_attention.argtypes = [vp, vp] + L.fp8kv_paged_attention.argtypes
         L.fp8kv_paged_attention_noalloc.restype = i32
         L.fp8kv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                                     i32, i32, i32, vp, vp, f32, i32, i32, vp, vp]
@@ -179,6 +181,36 @@ def fp8kv_paged_attention(q, k_cache, v_cache, block_table, seq_lens, max_seq_le
         _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
         workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
     _check("fp8kv_paged_attention", rc)
+    return out
+
+
+def fp8kv_append_paged_attention(k_new, v_new, q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale,
+                                 v_scale, sm_scale, window_left=-1, split_tokens=0, workspace=None, out=None,
+                                 num_pages=None, stream=None):
+    """fp8kv_paged_attention after writing the M new tokens of each sequence
+    (k_new, v_new bf16 [B][M][Hkv][D]) to the cache at positions L - M + m."""
+    dt = _cache_dtype(k_cache)
+    _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16)
+    _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
+    _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
+    B, M, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_cache.shape
+    if tuple(k_new.shape) != (B, M, Hkv, D) or tuple(v_new.shape) != (B, M, Hkv, D):
+        raise ValueError("k_new, v_new must be [B][M][Hkv][D]")
+    if num_pages is None:
+        num_pages = P
+    need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                                split_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib().fp8kv_append_paged_attention(
+        _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), int(max_seq_len), B, M, Hq, Hkv, D, page_size, int(num_pages),
+        _ptr(k_scale), _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
+        workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
+    _check("fp8kv_append_paged_attention", rc)
     return out
 
 
