@@ -318,18 +318,25 @@ def time_graphs(graphs, steps, warmup, stream):
 
 
 def capture_step_graphs(w: Workload, stream):
+    """One CUDA graph per cache copy; also returns the kernel launches one
+    step makes (counted by the library while the first graph is captured)."""
+    from verify_attention_gb300 import fp8kv
     graphs = []
     with torch.cuda.stream(stream):
         for c in range(len(w.copies)):
             w.step(c)                  # warm: attributes, tensor maps, lazy loading
     torch.cuda.synchronize()
+    launches = None
     for c in range(len(w.copies)):
         g = torch.cuda.CUDAGraph()
+        n0 = fp8kv.fp8kv_launch_count()
         with torch.cuda.graph(g, stream=stream):
             w.step(c)
+        if launches is None:
+            launches = fp8kv.fp8kv_launch_count() - n0
         graphs.append(g)
     torch.cuda.synchronize()
-    return graphs
+    return graphs, launches
 
 
 def dominant_kernel(w: Workload, stream, reps=24):
@@ -568,7 +575,7 @@ def main():
 
     ps = args.page_size if args.workload == "verify48" else (64 if args.workload == "decode128k" else 32)
     w = build_workload(args.workload, ps, dev, layers=args.layers)
-    graphs = capture_step_graphs(w, stream)
+    graphs, launches_per_step = capture_step_graphs(w, stream)
     fp8kv.fp8kv_device_status(clear=True)
 
     barrier(ws)
@@ -602,7 +609,8 @@ def main():
         "pct_of_hbm_roofline": value / ws / hbm_peak,
         "algorithmic_bytes_per_step": step_bytes,
         "useful_flops_per_step": w.flops_per_step(),
-        "gpu_launches": args.steps * sum(1 + 1 + (1 if l.ws_bytes else 0) for l in w.copies[0]),
+        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches_per_step": launches_per_step,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": "fp8kv_paged_attention (partial + reduce) on the largest layer",
@@ -617,7 +625,7 @@ def main():
         # the long-context decode gate: its own step and dominant kernel
         del graphs
         w2 = build_workload("decode128k", 64, dev)
-        g2 = capture_step_graphs(w2, stream)
+        g2, _ = capture_step_graphs(w2, stream)
         s2 = time_graphs(g2, 5, 3, stream) / 5
         b2, t2, _, d2 = dominant_kernel(w2, stream, reps=12)
         line["decode128k"] = {"gbs_step": w2.bytes_per_step() / s2 / 1e9, "ms_per_step": s2 * 1e3,

@@ -274,6 +274,10 @@ const char* fp8kv_status_string(int status);
  * full length. */
 int fp8kv_last_dispatch(char* buf, size_t n);
 
+/* Number of kernel launches this library has made in this process (all
+ * threads, all devices), e.g. the launches one step captures into a graph. */
+unsigned long long fp8kv_launch_count(void);
+
 /* Read (and with clear != 0, reset) the device status word of the current
  * device.  Synchronises the device.  Returns FP8KV_OK or FP8KV_ERR_CUDA. */
 int fp8kv_device_status(unsigned int* status, int clear);

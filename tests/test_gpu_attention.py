@@ -256,7 +256,8 @@ def test_empty_batch_launches_nothing():
     ([130, 33], 12, 32, 40, 64),         # mma.sync kernel with the append kernel
     ([500, 33], 1, 64, None, 0),         # decode kernel with the append kernel
 ])
-def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split):
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split, dtype):
     """fp8kv_append_paged_attention == fp8kv_cache_insert of the new rows at
     their slots followed by fp8kv_paged_attention: identical cache bytes and
     identical outputs, and within tolerance of the oracle."""
@@ -264,7 +265,10 @@ def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split):
     case = gen.layer_case(9500 + sum(seq_lens) + M + split, seq_lens, M, ps, window=window)
     lay = case.layout
     shape = (lay.num_pages, 8, ps, 128)
-    kc = torch.full(shape, 0xA5, dtype=torch.uint8, device="cuda")
+    if dtype == "e4m3":
+        kc = torch.full(shape, 0xA5, dtype=torch.uint8, device="cuda")
+    else:
+        kc = torch.zeros(shape, dtype=torch.bfloat16, device="cuda")
     vc = kc.clone()
     ks = torch.tensor([case.k_scale], device="cuda")
     vs = torch.tensor([case.v_scale], device="cuda")
@@ -282,9 +286,12 @@ def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split):
     torch.cuda.synchronize()
     assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
     assert torch.equal(out, ref)
-    okc, ovc = oracle_caches(case)
-    assert np.array_equal(kc.cpu().numpy(), okc)
-    assert_close(out, oracle_attention(case, okc, ovc), f"append {seq_lens} M={M}")
+    if dtype == "e4m3":
+        okc, ovc = oracle_caches(case)
+        assert np.array_equal(kc.cpu().numpy(), okc)
+    else:
+        okc, ovc = oracle_caches(case, "bf16")
+    assert_close(out, oracle_attention(case, okc, ovc, cache_dtype=dtype), f"append {seq_lens} M={M} {dtype}")
 
 
 # ------------------------------------------------------------ the configs

@@ -1,6 +1,7 @@
 // api.cu -- status strings, device status word, dispatch record, device facts.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -10,6 +11,9 @@
 namespace fp8kv {
 
 static thread_local char g_dispatch[256] = "";
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_dispatch(const char* text) {
     strncpy(g_dispatch, text, sizeof g_dispatch - 1);
@@ -66,3 +70,5 @@ extern "C" int fp8kv_device_status(unsigned int* status, int clear) {
     *status = s;
     return FP8KV_OK;
 }
+
+extern "C" unsigned long long fp8kv_launch_count(void) { return fp8kv::g_launches.load(std::memory_order_relaxed); }

@@ -244,6 +244,9 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
 
 // Host-side helpers (api.cu).
 namespace fp8kv {
+// Counts every kernel launch the library makes (api.cu; fp8kv_launch_count).
+void count_launch();
+
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel in the stream is finishing; it must call pdl_wait()
 // before reading anything that kernel may have written.  cluster_x > 1
@@ -265,7 +268,9 @@ static inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cluster_x > 1 ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaSuccess) count_launch();
+    return e;
 }
 
 template <typename... KArgs, typename... Args>

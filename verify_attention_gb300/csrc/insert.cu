@@ -291,5 +291,6 @@ extern "C" int fp8kv_e4m3_encode_bits(uint32_t first, size_t n, uint8_t* out, vo
     const uint64_t threads_needed = (n + 7) / 8;
     const uint64_t blocks = (threads_needed + 255) / 256;
     encode_bits_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(first, (uint64_t)n, out);
+    count_launch();
     return launch_status();
 }

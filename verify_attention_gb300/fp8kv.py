@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_status_string.argtypes = [i32]
         L.fp8kv_last_dispatch.restype = i32
         L.fp8kv_last_dispatch.argtypes = [ctypes.c_char_p, sz]
+        L.fp8kv_launch_count.restype = ctypes.c_ulonglong
+        L.fp8kv_launch_count.argtypes = []
         L.fp8kv_device_status.restype = i32
         L.fp8kv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), i32]
         _lib = L
@@ -244,6 +246,11 @@ def fp8kv_last_dispatch() -> str:
     buf = ctypes.create_string_buffer(512)
     lib().fp8kv_last_dispatch(buf, 512)
     return buf.value.decode()
+
+
+def fp8kv_launch_count():
+    """Kernel launches the library has made in this process."""
+    return int(lib().fp8kv_launch_count())
 
 
 def fp8kv_device_status(clear: bool = False) -> int:
