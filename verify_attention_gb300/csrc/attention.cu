@@ -137,8 +137,11 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         bool ok = true;
         int issued = 0;
+        // page ids 32 at a time, the next batch loaded while this one is issued
+        int next = (lane < n_pages) ? bt[lane] : 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
-            const int mine = (base + lane < n_pages) ? bt[base + lane] : 0;
+            const int mine = next;
+            if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
             const int cnt = min(32, n_pages - base);
             for (int j = 0; j < cnt; ++j) {
                 const int phys = __shfl_sync(0xffffffffu, mine, j);

@@ -207,8 +207,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         int issued = 0;
         bool new_seen = false;
+        // page ids 32 at a time, the next batch loaded while this one is issued
+        int next = (lane < n_pages) ? bt[lane] : 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
-            const int mine = (base + lane < n_pages) ? bt[base + lane] : 0;
+            const int mine = next;
+            if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
             const int cnt = min(32, n_pages - base);
             for (int j = 0; j < cnt; ++j) {
                 const int phys = __shfl_sync(0xffffffffu, mine, j);
