@@ -140,6 +140,22 @@ def test_plan_and_workspace_host_logic(L):
         fp8kv.fp8kv_paged_attention_plan(1, 1, 72, 8, 128, 64, 1000, -1, 100)
 
 
+def test_automatic_plans(L):
+    """The automatic partition policy on a 152-SM GB300 (the planning default
+    without a device): one wave of partitions for one long sequence of
+    verifier rows, one tile per partition (a cluster) when it spans at most
+    8 tiles, one CTA per SM for decode, quarters of the longest sequence for a
+    large batch."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("plans depend on the device's SM count")
+    plan = fp8kv.fp8kv_paged_attention_plan
+    assert plan(1, 12, 72, 8, 128, 32, 8192, -1, 0) == (16, 512)     # 19 partitions max per head, whole tiles
+    assert plan(1, 12, 72, 8, 128, 32, 8192, 511, 0) == (5, 128)     # window: 5 tiles -> 5-CTA cluster
+    assert plan(1, 1, 72, 8, 128, 64, 131072, -1, 0) == (19, 6912)   # decode: 19 x 8 = 152 CTAs
+    assert plan(64, 12, 72, 8, 128, 32, 32768, -1, 0) == (4, 8192)   # batch: a quarter of 32768
+
+
 def test_binding_rejects_cpu_tensors():
     k = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
