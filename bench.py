@@ -234,6 +234,15 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
         desc = (f"12 global layers, B=1, M=1, Hq=72, Hkv=8, D=128, L=131072, page 64, "
                 f"{cache_dtype} cache; per layer 1-token insert + split-KV attention + reduce")
         return Workload(name, copies, desc, 1)
+    if name == "prefill16k":
+        copies = [[]]
+        for l in range(layers or 4):
+            c = gen.layer_case(1006 * 100 + l, [16384], 1024, 64, window=None, device=device)
+            copies[0].append(Layer(c, device, split_tokens=0))
+            _free_context([c])
+        desc = ("4 global layers, B=1, a prefill chunk of M=1024 tokens at the end of L=16384, Hq=72, Hkv=8, "
+                "D=128, page 64, E4M3 cache; per layer 1024-token append + causal attention in 128-row tiles")
+        return Workload(name, copies, desc, 1024)
     if name == "serving64":
         lens = gen.cfg5_seq_lens()
         built = []
@@ -378,32 +387,57 @@ def flops_of(layer):
     return layer.flops()
 
 
+def _packed(tensors, device, align=256, pin=False):
+    """One byte buffer with room for `tensors` back to back (each start
+    aligned to `align` bytes) and views of it with their shapes and dtypes."""
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += -(-t.numel() * t.element_size() // align) * align
+    buf = torch.empty(max(n, align), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
+    return buf, views
+
+
 def e2e_measure(w: Workload, steps, stream):
-    """Through the public API with host buffers: per step, copy every layer's
-    new tokens and queries from pinned host memory, run the step's calls, and
-    read every attention output back into pinned host memory.  The step is
-    captured once in a CUDA graph (copies included) and replayed, as a serving
-    loop would run it; the same step launched eagerly from Python is timed too
-    (`eager_ms_per_step`: binding and launch overhead included)."""
+    """Through the public API with host buffers: per step, one copy of every
+    layer's new tokens and queries from a pinned host buffer, the step's
+    calls, and one copy of every layer's attention output back into pinned
+    host memory (the layers read and write views of the two device staging
+    buffers).  The step is captured once in a CUDA graph (copies included)
+    and replayed, as a serving loop would run it; the same step launched
+    eagerly from Python is timed too (`eager_ms_per_step`: binding and launch
+    overhead included).  Returns the outputs' agreement with the device-timed
+    step's outputs (same inputs and cache, same kernels: bit-identical)."""
     layers = w.copies[0]
-    host_in = []
-    h2d = d2h = 0
-    for l in layers:
-        srcs = [l.q, l.k_new, l.v_new] if l.fused is None else [l.fq, l.fk, l.fv, l.fpos, l.fslots]
-        hs = [t.cpu().pin_memory() for t in srcs]
-        host_in.append((hs, srcs))
-        h2d += sum(t.numel() * t.element_size() for t in hs)
-    host_out = [torch.empty(l.out.shape, dtype=l.out.dtype).pin_memory() for l in layers]
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    dev = layers[0].q.device
+    names = [["q", "k_new", "v_new"] if l.fused is None else ["fq", "fk", "fv", "fpos", "fslots"] for l in layers]
+    saved_in = [[getattr(l, n) for n in ns] for l, ns in zip(layers, names)]
+    saved_out = [l.out for l in layers]
+    flat_in = [t for ts in saved_in for t in ts]
+    dev_in, dviews = _packed(flat_in, dev)
+    host_in, hviews = _packed(flat_in, "cpu", pin=True)
+    for h, t in zip(hviews, flat_in):
+        h.copy_(t)
+    dev_out, oviews = _packed(saved_out, dev)
+    host_out, hoviews = _packed(saved_out, "cpu", pin=True)
+    h2d, d2h = host_in.numel(), host_out.numel()
+    it = iter(dviews)
+    for l, ns in zip(layers, names):
+        for n in ns:
+            setattr(l, n, next(it))
+    for l, o in zip(layers, oviews):
+        l.out = o
     torch.cuda.synchronize()
 
     def one():
         with torch.cuda.stream(stream):
-            for (hs, ds), l, ho in zip(host_in, layers, host_out):
-                for h, d in zip(hs, ds):
-                    d.copy_(h, non_blocking=True)
+            dev_in.copy_(host_in, non_blocking=True)
+            for l in layers:
                 l.step(w.ws)
-                ho.copy_(l.out, non_blocking=True)
+            host_out.copy_(dev_out, non_blocking=True)
 
     def timed(run, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -414,27 +448,36 @@ def e2e_measure(w: Workload, steps, stream):
         b.synchronize()
         return a.elapsed_time(b) / 1e3 / n
 
-    one()
-    torch.cuda.synchronize()
-    eager_s = timed(one, steps)
     try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            one()
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g.replay()
+        one()
         torch.cuda.synchronize()
-    except RuntimeError as e:          # a torch without host-copy capture: eager only
-        torch.cuda.synchronize()
-        return eager_s, eager_s, h2d, d2h, f"eager launches (graph capture of the copies failed: {e})"[:200]
+        match = all(torch.equal(h, o.cpu()) for h, o in zip(hoviews, saved_out))
+        eager_s = timed(one, steps)
+        mode = "step captured in a CUDA graph with one pinned-host copy in and one out, replayed"
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                one()
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+            torch.cuda.synchronize()
 
-    def replay():
-        with torch.cuda.stream(stream):
-            g.replay()
-    graph_s = timed(replay, steps)
-    del g
-    return graph_s, eager_s, h2d, d2h, "step captured in a CUDA graph with its pinned-host copies, replayed"
+            def replay():
+                with torch.cuda.stream(stream):
+                    g.replay()
+            graph_s = timed(replay, steps)
+            del g
+        except RuntimeError as e:      # a torch without host-copy capture: eager only
+            torch.cuda.synchronize()
+            graph_s, mode = eager_s, f"eager launches (graph capture of the copies failed: {e})"[:200]
+    finally:
+        for l, ns, ts in zip(layers, names, saved_in):
+            for n, t in zip(ns, ts):
+                setattr(l, n, t)
+        for l, o in zip(layers, saved_out):
+            l.out = o
+    return graph_s, eager_s, h2d, d2h, mode, match
 
 
 # ---------------------------------------------------------- CPU oracle leg
@@ -445,6 +488,8 @@ def oracle_case(name, page_size):
         return gen.cfg3_case(3, page_size)
     if name == "decode128k":
         return gen.cfg4_case(0)
+    if name == "prefill16k":
+        return gen.layer_case(1006 * 100, [16384], 1024, 64, window=None)
     return gen.cfg5_case(0)
 
 
@@ -497,8 +542,9 @@ class OracleSample:
 
 def cpu_baseline(name, page_size, target_s=12.0):
     s = OracleSample(name, page_size)
-    b, t = s.run(s.G * s.case.M)                          # one KV head's rows: calibration
-    n = int(min(len(s.rows_all), max(1, s.G * s.case.M * target_s / max(t, 1e-3))))
+    n0 = min(s.G * s.case.M, 256)
+    b, t = s.run(n0)                                      # up to one KV head's rows: calibration
+    n = int(min(len(s.rows_all), max(1, n0 * target_s / max(t, 1e-3))))
     b, t = s.run(n)
     return {"value": b / t / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": s.describe(n) + f"; host has {os.cpu_count()} cores"}
@@ -577,7 +623,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="verify48", choices=["verify48", "decode128k", "serving64"])
+    ap.add_argument("--workload", default="verify48", choices=["verify48", "decode128k", "serving64",
+                                                                  "prefill16k"])
     ap.add_argument("--page-size", type=int, default=32, choices=[32, 64])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -595,9 +642,10 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.Stream(device=dev)
-    hbm_peak, _, peak_src = peaks()
+    hbm_peak, bf16_peak, peak_src = peaks()
 
-    ps = args.page_size if args.workload == "verify48" else (64 if args.workload == "decode128k" else 32)
+    ps = args.page_size if args.workload == "verify48" else (64 if args.workload in ("decode128k", "prefill16k")
+                                                             else 32)
     w = build_workload(args.workload, ps, dev, layers=args.layers)
     graphs, launches_per_step = capture_step_graphs(w, stream)
     fp8kv.fp8kv_device_status(clear=True)
@@ -620,7 +668,7 @@ def main():
     dom_bytes, dom_s, dom_flops, dispatch = dominant_kernel(w, stream)
     achieved = dom_bytes / dom_s / 1e9
     traffic, traffic_note = measured_traffic(dispatch)
-    e2e_s, e2e_eager_s, h2d, d2h, e2e_mode = e2e_measure(w, max(3, min(args.steps, 20)), stream)
+    e2e_s, e2e_eager_s, h2d, d2h, e2e_mode, e2e_match = e2e_measure(w, max(3, min(args.steps, 20)), stream)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -644,9 +692,18 @@ def main():
         "e2e": {"value": ws * step_bytes / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
                 "mode": e2e_mode,
-                "eager_ms_per_step": e2e_eager_s * 1e3},
+                "eager_ms_per_step": e2e_eager_s * 1e3, "outputs_match_device_step": e2e_match},
         "clocks": clk.summary(),
     }
+    if args.workload == "prefill16k":
+        # a prefill chunk is bound by the tensor cores: useful FLOPs against the
+        # measured dense bf16 peak (P.V runs in f16, Q.K^T as two E4M3 terms)
+        tf = dom_flops / dom_s / 1e12
+        line["roofline"].update({"bound": "tensor", "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                                 "frac": tf / bf16_peak, "traffic": None,
+                                 "traffic_source": "no capture for this kernel and workload",
+                                 "gbs": achieved,
+                                 "peak_source": f"{peak_src} bf16_tflops (MEASURED_PEAKS.json)"})
     if rank == 0 and args.workload == "verify48" and not args.no_extra:
         # the long-context decode gate: its own step and dominant kernel
         del graphs
@@ -658,6 +715,15 @@ def main():
                               "attention_gbs": b2 / t2 / 1e9, "attention_frac": b2 / t2 / 1e9 / hbm_peak,
                               "attention_ms": t2 * 1e3, "dispatch": d2}
         del g2, w2
+        # a prefill chunk on the same kernel (row tiles): bound by the tensor cores
+        w3 = build_workload("prefill16k", 64, dev)
+        g3, _ = capture_step_graphs(w3, stream)
+        s3 = time_graphs(g3, 5, 3, stream) / 5
+        _, t3, f3, d3 = dominant_kernel(w3, stream, reps=8)
+        line["prefill16k"] = {"ms_per_step": s3 * 1e3, "tflops_step": w3.flops_per_step() / s3 / 1e12,
+                              "attention_ms": t3 * 1e3, "attention_tflops": f3 / t3 / 1e12,
+                              "attention_frac_of_bf16_peak": f3 / t3 / 1e12 / bf16_peak, "dispatch": d3}
+        del g3, w3
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, ps)
     if rank == 0:

@@ -186,9 +186,14 @@ size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D
  *                may be NULL when that size is 0; contents need no
  *                initialisation and are scratch after the call
  *   out          (device) bf16 [B][M][Hq][D]
- * Supported: D = 128, page_size 32 or 64, 1 <= M <= 16, Hq % Hkv == 0,
- * M * (Hq/Hkv) <= 144.  B = 0 launches nothing and returns FP8KV_OK without
- * reading any pointer.
+ * Supported: D = 128, page_size 32 or 64, Hq % Hkv == 0, and either
+ * 1 <= M <= 16 with M * (Hq/Hkv) <= 144 rows per KV head (any cache type), or
+ * up to M = 16384 query rows per sequence on an E4M3 cache with partitions of
+ * whole 128-key tiles (split_tokens 0 or a multiple of 128): a prefill chunk
+ * at the end of the context, causal within the chunk, on the tcgen05 kernel
+ * in 128-row tiles (Hkv * ceil(M * Hq/Hkv / 128) <= 65535); other shapes
+ * return FP8KV_ERR_UNSUPPORTED.  B = 0 launches nothing and returns FP8KV_OK
+ * without reading any pointer.
  * Device checks: seq_len < M, seq_len > max_seq_len or more pages than
  * max_pages_per_seq -> that sequence's output is left untouched
  * (FP8KV_DEV_BAD_SEQ_LEN); page ids outside [0, num_pages) read zeros.
@@ -213,9 +218,10 @@ int fp8kv_paged_attention(const void* q, const void* k_cache, const void* v_cach
  * fp8kv_cache_insert encoding; then fp8kv_paged_attention runs with the same
  * arguments.  Cache bytes and output are identical to fp8kv_cache_insert
  * with those slots followed by fp8kv_paged_attention.  On the tensor-memory
- * path the CTA whose partition holds a new position writes it before
- * loading that page (no separate insert launch); otherwise an append kernel
- * runs first.  k_new and v_new must be 16-byte aligned; B = 0 is a no-op.
+ * path with one 128-row tile per KV head the CTA whose partition holds a new
+ * position writes it before loading that page (no separate insert launch);
+ * otherwise (a prefill chunk in several row tiles, or the mma.sync kernels)
+ * an append kernel runs first.  k_new and v_new must be 16-byte aligned; B = 0 is a no-op.
  * Device check: a block-table entry outside [0, num_pages) at a new
  * position -> that token is not written (FP8KV_DEV_BAD_SLOT).
  */

@@ -68,6 +68,12 @@ def test_attention_validation(L):
     assert _attn(L, M=0) == E_INV
     assert _attn(L, Hq=70) == E_INV                 # not a multiple of Hkv
     assert _attn(L, M=16, Hq=80) == E_UNS           # 16 x 10 rows > 144
+    # more than 16 rows per sequence or 144 per KV head: E4M3 cache and whole
+    # 128-key partitions only (the tcgen05 kernel's row tiles)
+    assert _attn(L, M=17, dt=1, split=0) == E_UNS
+    assert _attn(L, M=16, Hq=80, dt=1, split=0) == E_UNS
+    assert _attn(L, M=40, split=96) == E_UNS
+    assert _attn(L, M=16385, split=0) == E_UNS
     assert _attn(L, split=48) == E_INV              # not a multiple of the page size
     assert _attn(L, maxL=200) == E_INV              # beyond max_pages_per_seq * page_size
     assert _attn(L, dt=7) == E_INV
@@ -133,6 +139,13 @@ def test_plan_and_workspace_host_logic(L):
     assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 4096) == 0
     assert fp8kv.fp8kv_paged_attention_workspace_size(1, 12, 72, 8, 128, 64, 4096, -1, 2048) == \
         1 * 12 * 72 * 2 * 130 * 4
+    # a prefill chunk of 512 tokens (36 row tiles of 128 rows per KV head):
+    # 288 units fill the SMs, one partition each; one KV head of a short chunk
+    # gets partitions of at least 1024 keys (whole 128-key tiles)
+    ns, st = fp8kv.fp8kv_paged_attention_plan(1, 512, 72, 8, 128, 64, 8192, -1, 0)
+    assert (ns, st) == (1, 8192)
+    ns, st = fp8kv.fp8kv_paged_attention_plan(1, 32, 9, 1, 128, 32, 32768, -1, 0)
+    assert st % 128 == 0 and st >= 1024 and ns == -(-32768 // st)
     # a window of 512 with 12 rows spans at most ceil(523/64)+1 = 10 pages of 64
     ns, st = fp8kv.fp8kv_paged_attention_plan(1, 12, 72, 8, 128, 64, 8192, 511, 64)
     assert ns == 10

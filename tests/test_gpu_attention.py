@@ -294,6 +294,77 @@ def test_append_equals_insert_then_attention(seq_lens, M, ps, window, split, dty
     assert_close(out, oracle_attention(case, okc, ovc, cache_dtype=dtype), f"append {seq_lens} M={M} {dtype}")
 
 
+# ---------------------------------------------- prefill-shaped row counts
+
+PREFILL = [
+    # seq_lens, M, ps, window
+    ([1024], 256, 32, None),          # 2304 rows per KV head: 18 row tiles
+    ([600, 300], 130, 64, 127),       # 1170 rows: 10 tiles, the last of 18 rows; sliding
+    ([200], 200, 32, None),           # the whole sequence is new (L = M): causal from key 0
+    ([777], 64, 64, 300),             # 576 rows, a window shorter than the chunk
+]
+
+
+@pytest.mark.parametrize("seq_lens,M,ps,window", PREFILL)
+def test_prefill_row_tiles(seq_lens, M, ps, window):
+    """More than 16 query rows per sequence (a chunk of M tokens at the end of
+    the context): the tcgen05 kernel in 128-row tiles, each loading the keys
+    its rows see (causal within the chunk, window), automatic and explicit
+    partitions."""
+    case = gen.layer_case(9700 + sum(seq_lens) + M, seq_lens, M, ps, window=window)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    ref = oracle_attention(case, okc, ovc)
+    tiles = -(-M * 9 // 128)
+    for st in (0, 128, 384):
+        out = gpu_attention(case, kc, vc, ks, vs, split_tokens=st)
+        d = fp8kv().fp8kv_last_dispatch()
+        assert d.startswith("attention_tc") and f"row_tiles={tiles} " in d, d
+        assert_close(out, ref, f"prefill {seq_lens} M={M} split={st}")
+
+
+def test_prefill_rows_need_e4m3_cache_and_whole_tiles():
+    """Prefill row counts run only on the tcgen05 kernel: a BF16 cache or
+    partitions that are not whole 128-key tiles are refused, not served slowly."""
+    f = fp8kv()
+    case = gen.layer_case(9750, [300], 40, 32)
+    kc, vc, ks, vs = gpu_caches(case, "bf16")
+    with pytest.raises(f.Fp8kvError):
+        gpu_attention(case, kc, vc, ks, vs)
+    kc, vc, ks, vs = gpu_caches(case)
+    with pytest.raises(f.Fp8kvError):
+        gpu_attention(case, kc, vc, ks, vs, split_tokens=96)
+
+
+def test_prefill_append_equals_insert_then_attention():
+    """A prefill chunk through the append entry (the append kernel, then the
+    row-tiled attention): cache bytes of the insert, bit-identical output,
+    within tolerance of the oracle."""
+    from verify_attention_gb300 import fp8kv as f
+    seq_lens, M, ps = [900, 400], 300, 32
+    case = gen.layer_case(9760, seq_lens, M, ps)
+    lay = case.layout
+    kc = torch.full((lay.num_pages, 8, ps, 128), 0xA5, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    ks = torch.tensor([case.k_scale], device="cuda")
+    vs = torch.tensor([case.v_scale], device="cuda")
+    f.fp8kv_cache_insert(case.k_prior.cuda(), case.v_prior.cuda(), case.slots_prior.cuda(), ks, vs, kc, vc)
+    kc2, vc2 = kc.clone(), vc.clone()
+    f.fp8kv_cache_insert(case.k_new.cuda(), case.v_new.cuda(), case.slots_new.cuda(), ks, vs, kc2, vc2)
+    ref = gpu_attention(case, kc2, vc2, ks, vs)
+    B = len(seq_lens)
+    out = f.fp8kv_append_paged_attention(case.k_new.cuda().view(B, M, 8, 128), case.v_new.cuda().view(B, M, 8, 128),
+                                         case.q.cuda(), kc, vc, lay.block_table.cuda(), lay.seq_lens.cuda(),
+                                         int(lay.seq_lens.max()), ks, vs, case.sm_scale)
+    torch.cuda.synchronize()
+    assert "row_tiles=22 " in f.fp8kv_last_dispatch()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(out, ref)
+    okc, ovc = oracle_caches(case)
+    assert np.array_equal(kc.cpu().numpy(), okc)
+    assert_close(out, oracle_attention(case, okc, ovc), "prefill append")
+
+
 # ------------------------------------------------------------ the configs
 
 def test_cfg1_tiny_decode():

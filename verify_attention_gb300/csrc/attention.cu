@@ -37,7 +37,8 @@ namespace fp8kv {
 
 int status_attention(unsigned int* s, int clear) { return read_status(s, clear); }
 
-constexpr int kMaxRowTiles = 9;          // M*G <= 144
+constexpr int kMaxRowTiles = 9;          // M*G <= 144 on the mma.sync kernels
+constexpr int kMaxM = 16384;             // query rows per sequence (prefill chunks; E4M3 cache)
 // Bytes of K/V stages per CTA for several row tiles; for the decode shape
 // (one row tile) the key groups, their stage budget and the register cap of
 // the decode kernel.  Overridable at build time for tuning sweeps.
@@ -531,9 +532,9 @@ __global__ void __maxnreg__(FP8KV_DECODE_REGS) paged_decode_kernel(
 __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restrict__ ws_o,
                                                           const float* __restrict__ ws_ml,
                                                           const int32_t* __restrict__ seq_lens, int B, int M,
-                                                          int Hq, int mpps, int page_size, int window_left,
-                                                          int split_pages, int num_splits, int max_seq_len,
-                                                          uint16_t* out) {
+                                                          int Hq, int G, int tile_rows, int mpps,
+                                                          int page_size, int window_left, int split_pages,
+                                                          int num_splits, int max_seq_len, uint16_t* out) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -542,8 +543,12 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     const int b = (int)(row / ((int64_t)M * Hq));
     const int L = seq_lens[b];
     if (L < M || L > max_seq_len || (L + page_size - 1) / page_size > mpps) return;
-    const int lo0 = (window_left >= 0) ? max(0, L - M - window_left) : 0;
-    const int first_page = lo0 / page_size, last_page = (L - 1) / page_size;
+    // the keys of this row's tile of tile_rows rows (row m * G + h % G of its
+    // KV head), split into partitions exactly as the attention kernel did
+    const int m = (int)(row / Hq % M), rk = m * G + (int)(row % Hq) % G;
+    const int R0 = rk / tile_rows * tile_rows, RL = min(tile_rows, M * G - R0);
+    const int lo0 = (window_left >= 0) ? max(0, L - M + R0 / G - window_left) : 0;
+    const int first_page = lo0 / page_size, last_page = (L - M + (R0 + RL - 1) / G) / page_size;
     const int ns = (last_page - first_page + split_pages) / split_pages;
     if (ns <= 1 || ns > num_splits) return;
     // partition weights: lane j owns partitions j, j+32, ...
@@ -647,23 +652,29 @@ struct Plan {
 
 static int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
+// 128-row tiles of the tcgen05 kernel per (sequence, KV head).
+static int row_tiles(int M, int Hq, int Hkv) { return ceil_div((int64_t)M * (Hq / Hkv), 128); }
+
 static int check_sizes(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_len, int window_left,
                        int split_tokens) {
     if (B < 0 || M < 1 || Hq <= 0 || Hkv <= 0 || max_seq_len < 0 || window_left < -1 || split_tokens < 0)
         return FP8KV_ERR_INVALID_ARG;
     if (Hq % Hkv) return FP8KV_ERR_INVALID_ARG;
-    if (D != 128 || (PS != 32 && PS != 64) || M > 16) return FP8KV_ERR_UNSUPPORTED;
-    if (M * (Hq / Hkv) > 16 * kMaxRowTiles) return FP8KV_ERR_UNSUPPORTED;
+    if (D != 128 || (PS != 32 && PS != 64) || M > kMaxM) return FP8KV_ERR_UNSUPPORTED;
+    // more than 16 rows per sequence or 144 per KV head: the row tiles of the
+    // tcgen05 kernel (E4M3 cache, checked with the cache type)
+    if ((int64_t)Hkv * row_tiles(M, Hq, Hkv) > 65535) return FP8KV_ERR_UNSUPPORTED;
     if (split_tokens % PS) return FP8KV_ERR_INVALID_ARG;
     if (B > 65535 || Hkv > 65535) return FP8KV_ERR_UNSUPPORTED;
     return FP8KV_OK;
 }
 
-// Rows per KV head served by the tcgen05 kernel (on an E4M3 cache).
-static bool tc_rows(int M, int Hq, int Hkv) {
-    const int R = M * (Hq / Hkv);
-    return R > 16 && R <= 128;
-}
+// Rows per KV head served by the tcgen05 kernel (on an E4M3 cache): more
+// than 16, in tiles of 128.
+static bool tc_rows(int M, int Hq, int Hkv) { return (int64_t)M * (Hq / Hkv) > 16; }
+
+// Shapes only the tcgen05 kernel serves: prefill-like row counts.
+static bool tc_only(int M, int Hq, int Hkv) { return M > 16 || (int64_t)M * (Hq / Hkv) > 16 * kMaxRowTiles; }
 
 static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_len, int window_left,
                      int split_tokens, Plan* p) {
@@ -672,34 +683,42 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
     // pages spanned by the visible keys of the longest sequence
     int pages = ceil_div(max(max_seq_len, 1), PS);
     if (window_left >= 0) pages = min(pages, ceil_div((int64_t)M + window_left, PS) + 1);
+    const int RT = tc_rows(M, Hq, Hkv) ? row_tiles(M, Hq, Hkv) : 1;
     int sp;
     if (split_tokens > 0) {
         sp = split_tokens / PS;
     } else {
-        // one (decode: a single row tile, one CTA per SM) or two partitions
-        // per SM over all (sequence, head) units, with at least 1024 keys per
-        // partition: per-CTA set-up and the partial write-back make short
-        // partitions expensive
-        const int64_t units = (int64_t)max(B, 1) * Hkv;
-        const int64_t target = (M * (Hq / Hkv) <= 16 ? 1LL : 2LL) * num_sms();
+        // one (decode: a single row tile, one CTA per SM; prefill: several
+        // row tiles) or two partitions per SM over all (sequence, head, row
+        // tile) units, with at least 1024 keys per partition: per-CTA set-up
+        // and the partial write-back make short partitions expensive
+        const int64_t units = (int64_t)max(B, 1) * Hkv * RT;
+        const int64_t target = (M * (Hq / Hkv) <= 16 || RT > 1 ? 1LL : 2LL) * num_sms();
         const int per = (int)std::max<int64_t>(1, (target + units - 1) / units);
         sp = max(ceil_div(pages, per), 1024 / PS);
         // with many units and long sequences, at least four partitions per
         // sequence keep the longest ones from holding an SM alone at the end
         // of the launch (sequence lengths are only known on the device)
-        if (ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
+        // (prefill row tiles are many units already, and every partition
+        // writes a partial per row)
+        if (RT == 1 && ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
         // one sequence of verifier rows (one CTA per SM): at most 8 tiles of
         // 128 keys get a tile per partition (the partitions of a KV head then
         // run as one thread-block cluster and combine on chip); longer ones
         // one wave of partitions over the SMs, whole tiles each
-        if (B == 1 && tc_rows(M, Hq, Hkv)) {
+        if (B == 1 && tc_rows(M, Hq, Hkv) && RT == 1) {
             const int tile_pages = max(1, tc_tile_tokens() / PS);
             const int tiles = ceil_div(pages, tile_pages);
             const int wave = max(1, num_sms() / Hkv);
             sp = tiles <= 8 ? tile_pages : tile_pages * ceil_div(tiles, min(tiles, wave));
         }
     }
-    sp = max(1, min(sp, pages));
+    if (sp > pages) {
+        // one partition: whole 128-key tiles still when the request had them
+        const int tp = max(1, tc_tile_tokens() / PS);
+        sp = (sp % tp == 0) ? ceil_div(pages, tp) * tp : pages;
+    }
+    sp = max(1, sp);
     // automatic partitions hold whole 128-key tiles of the tensor-memory kernel
     if (split_tokens == 0) {
         const int tile_pages = tc_tile_tokens() / PS;
@@ -784,6 +803,11 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     Plan plan;
     int rc = make_plan(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left, split_tokens, &plan);
     if (rc) return rc;
+    // more than 16 query rows per KV head on E4M3 pages, partitions of whole
+    // 128-key tiles: tcgen05 kernel (128-row MMA tiles); otherwise mma.sync,
+    // which serves at most 16 rows per sequence and 144 per KV head
+    const bool use_tc = fp8 && tc_rows(M, Hq, Hkv) && (plan.split_tokens % tc_tile_tokens()) == 0;
+    if (!use_tc && tc_only(M, Hq, Hkv)) return FP8KV_ERR_UNSUPPORTED;
     if (B == 0) return FP8KV_OK;                                // nothing to do; no pointer is read
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return FP8KV_ERR_INVALID_ARG;
     if ((k_new != nullptr) != (v_new != nullptr) || (k_new && (!al16(k_new) || !al16(v_new))))
@@ -821,7 +845,8 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     P.G = Hq / Hkv;
     P.R = M * P.G;
     P.NT = (P.R + 15) / 16;
-    {
+    P.KW = P.SG = 1;
+    if (P.NT <= kMaxRowTiles) {
         // key groups split a partition's pages when one row tile leaves warps
         // idle; each group keeps at least two stages in flight when it can
         const int stages = page_size == 32 ? (fp8 ? Cfg<32, true>::kStages : Cfg<32, false>::kStages)
@@ -846,13 +871,12 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     P.max_seq_len = max_seq_len;
 
     cudaStream_t s = (cudaStream_t)stream;
-    // up to 128 query rows per KV head on E4M3 pages, partitions of whole
-    // 128-key tiles: tcgen05 kernel (one 128-row MMA tile); otherwise mma.sync
-    const bool use_tc = fp8 && tc_rows(M, Hq, Hkv) && (plan.split_tokens % tc_tile_tokens()) == 0;
-    // one sequence in at most 8 partitions: the partitions of a KV head run
-    // as one thread-block cluster and combine in distributed shared memory
-    P.cluster = (use_tc && B == 1 && plan.num_splits > 1 && plan.num_splits <= 8) ? plan.num_splits : 0;
-    if (k_new && use_tc) {                                          // appended in the kernel
+    const int RT = use_tc ? row_tiles(M, Hq, Hkv) : 1;
+    // one sequence in at most 8 partitions and one row tile: the partitions
+    // of a KV head run as one thread-block cluster and combine in distributed
+    // shared memory
+    P.cluster = (use_tc && B == 1 && RT == 1 && plan.num_splits > 1 && plan.num_splits <= 8) ? plan.num_splits : 0;
+    if (k_new && use_tc && RT == 1) {                               // appended in the kernel
         P.k_new = (const uint16_t*)k_new;
         P.v_new = (const uint16_t*)v_new;
         P.k_cache = (uint8_t*)k_cache;
@@ -873,9 +897,9 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     if (plan.num_splits > 1 && P.cluster <= 1) {
         const int64_t warps = (int64_t)B * M * Hq;
         cudaError_t e = launch_pdl(attn_reduce_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
-                                   (const float*)P.ws_o, (const float*)P.ws_ml, seq_lens, B, M, Hq,
-                                   max_pages_per_seq, page_size, window_left, plan.split_pages, plan.num_splits,
-                                   max_seq_len, (uint16_t*)out);
+                                   (const float*)P.ws_o, (const float*)P.ws_ml, seq_lens, B, M, Hq, P.G,
+                                   use_tc ? 128 : P.R, max_pages_per_seq, page_size, window_left,
+                                   plan.split_pages, plan.num_splits, max_seq_len, (uint16_t*)out);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return FP8KV_ERR_CUDA;
@@ -884,9 +908,9 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     char buf[256];
     if (use_tc)
         snprintf(buf, sizeof buf,
-                 "attention_tc<ps=%d,e4m3> rows=%d tile=128x128 splits=%d split_tokens=%d grid=%dx%dx%d threads=%d "
-                 "cluster=%d reduce=%d",
-                 page_size, P.R, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv, B, tc_threads(),
+                 "attention_tc<ps=%d,e4m3> rows=%d row_tiles=%d tile=128x128 splits=%d split_tokens=%d "
+                 "grid=%dx%dx%d threads=%d cluster=%d reduce=%d",
+                 page_size, P.R, RT, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv * RT, B, tc_threads(),
                  P.cluster > 1 ? P.cluster : 1, (plan.num_splits > 1 && P.cluster <= 1) ? 1 : 0);
     else
         snprintf(buf, sizeof buf,

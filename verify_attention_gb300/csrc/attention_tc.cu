@@ -1,6 +1,7 @@
 // attention_tc.cu -- paged verifier attention on the 5th-generation tensor
-// cores (tcgen05) for 17 to 128 query rows per KV head (M x G rows; the
-// M = 12 verifier has 108) of "Laguna S 2.1 INT4 --
+// cores (tcgen05) for more than 16 query rows per KV head (M x G rows; the
+// M = 12 verifier has 108, a prefill chunk of M tokens M x G in 128-row tiles,
+// one CTA per tile, each loading the keys its rows see) of "Laguna S 2.1 INT4 --
 // calibrated FP8 KV on Intel B70" ("Contract"; "Initial optimization order",
 // item 2: exact q1/M12 paged attention) over the E4M3 cache ("Laguna S 2.1
 // KV-cache precision decision", property table: "scale/dequantize or use native
@@ -17,7 +18,7 @@
 // memory and is the A operand, V is widened E4M3 -> f16 (exact) into a
 // swizzled MN-major tile.  Rows past M x G (up to 128) carry Q = 0.
 //
-// One CTA per (partition, KV head, sequence), 16 warps:
+// One CTA per (partition, row tile x KV head, sequence), 16 warps:
 //   warp 0          TMA producer (128-key tiles: K and V E4M3, 2 or 4 pages);
 //                   allocates and frees the tensor memory
 //   warp 1          MMA issuer (one thread); completion via tcgen05.commit
@@ -134,7 +135,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     uint32_t* tmem_slot = (uint32_t*)(bars + B_COUNT);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-    const int split = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    // blockIdx.y = row tile + RT * KV head: the row tiles of one head are
+    // neighbours in launch order and share its pages in L2
+    const int RT = (P.R + 127) >> 7;
+    const int split = blockIdx.x, rt = blockIdx.y % RT, hk = blockIdx.y / RT, b = blockIdx.z;
+    const int R0 = rt * 128, RL = min(128, P.R - R0);      // this CTA's rows R0 .. R0 + RL - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
 
@@ -180,9 +185,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     const int L = P.seq_lens[b];
     const bool seq_ok = !(L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps);
     bool run = seq_ok;                                      // uniform over the CTA
-    if (!seq_ok && threadIdx.x == 0 && split == 0 && hk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
-    const int lo0 = (P.window_left >= 0) ? max(0, L - P.M - P.window_left) : 0;
-    const int first_page = lo0 / PS, last_page = (L - 1) / PS;
+    if (!seq_ok && threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+    // keys visible to any row of the tile: from the first row's window start
+    // to the last row's position (row r is query m = r / G at L - M + m)
+    const int hi0 = L - P.M + (R0 + RL - 1) / P.G;
+    const int lo0 = (P.window_left >= 0) ? max(0, L - P.M + R0 / P.G - P.window_left) : 0;
+    const int first_page = lo0 / PS, last_page = hi0 / PS;
     const int nsplit_b = (last_page - first_page + P.split_pages) / P.split_pages;
     if (run && nsplit_b > P.num_splits) {
         if (threadIdx.x == 0 && split == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const int k0 = k_begin + t * NK;
             const int pages_here = min(PPT, n_pages - t * PPT);
             const int zlo = max(0, min(NK, lo0 - k0));
-            const int zhi = max(0, min(min(NK, pages_here * PS), L - k0));
+            const int zhi = max(0, min(min(NK, pages_here * PS), hi0 + 1 - k0));
             const uint8_t* src = stg + s * STG_BYTES + STG_K;
             uint8_t* dst = vbuf + vb * VBUF_BYTES;
             constexpr int PER = (NK * 8 + CONV_THREADS - 1) / CONV_THREADS;   // chunks per thread
@@ -379,9 +387,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // ------------------------------------------------------------ softmax
         const int wq = warp & 3, half = (warp - 4) >> 2;
         const int r = wq * 32 + lane;
-        const bool active = wq * 32 < P.R;                  // quarter holds at least one real row
+        const bool active = wq * 32 < RL;                   // quarter holds at least one real row
         const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-        const int rr = min(r, P.R - 1);
+        const int rr = R0 + min(r, RL - 1);                 // the row of the (b, hk) block
         const int m = rr / P.G;
         const int p_r = L - P.M + m;
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const float vs = *P.v_scale;
         // rows past M*G get Q = 0: their (unused) weights stay finite and their
         // lanes take the same unmasked path as the real rows
-        const bool pad = r >= P.R;
+        const bool pad = r >= RL;
         float mult;
         {
             // Q row split in place: q' = q * 2^sh with the row maximum |q'| in
@@ -587,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                                               __uint_as_float(ov[4 * v4 + 2]) * f, __uint_as_float(ov[4 * v4 + 3]) * f);
                 }
             }
-            if (r < P.R && !combine) {
+            if (r < RL && !combine) {
                 fence_proxy_async();        // the staged row, written by this thread, to the bulk copy
                 if (direct)
                     bulk_store(P.out + row_idx * 128 + 64 * half, smem_u32(row_stage), 128);
@@ -596,7 +604,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 bulk_commit();
                 bulk_wait_read();
             }
-            if (r < P.R && !direct && half == 0) {
+            if (r < RL && !direct && half == 0) {
                 if (combine) {
                     xch[r] = m_run;                         // the tile exchange area is free now
                     xch[128 + r] = l_tot;
@@ -619,7 +627,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         cluster_sync_all();
         if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
             const int hh = lane >> 4;                       // staged half row of these dims
-            for (int r = split + P.cluster * warp; r < P.R; r += P.cluster * WARPS) {
+            for (int r = split + P.cluster * warp; r < RL; r += P.cluster * WARPS) {
                 // every remote load of the row first (one round trip), then the arithmetic
                 const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 8;
                 uint2 v[8];
@@ -649,8 +657,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                     acc.w = fmaf(wp, c2.y, acc.w);
                 }
                 const float inv = *P.v_scale / lsum;
-                const int m = r / P.G;
-                const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + r % P.G;
+                const int m = (R0 + r) / P.G;
+                const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + r) % P.G;
                 *(uint2*)(P.out + orow * 128 + 4 * lane) =
                     make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
             }
@@ -674,7 +682,9 @@ int tc_tile_tokens() { return tc::NK; }
 int tc_threads() { return tc::THREADS; }
 
 int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& P, cudaStream_t s) {
-    if (P.R > 128 || P.R <= 16) return FP8KV_ERR_UNSUPPORTED;
+    const int RT = (P.R + 127) / 128;
+    if (P.R <= 16 || (int64_t)RT * P.Hkv > 65535) return FP8KV_ERR_UNSUPPORTED;
+    if (RT > 1 && (P.cluster > 1 || P.k_new)) return FP8KV_ERR_UNSUPPORTED;   // single row tile only
     if ((P.split_pages * P.page_size) % tc::NK) return FP8KV_ERR_UNSUPPORTED;
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
@@ -691,7 +701,7 @@ int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Attn
         }
     }
     cudaError_t e;
-    dim3 grid(P.num_splits, P.Hkv, P.B);
+    dim3 grid(P.num_splits, P.Hkv * RT, P.B);
     if (P.cluster > 1 && (P.cluster > 8 || P.cluster != P.num_splits)) return FP8KV_ERR_UNSUPPORTED;
     e = launch_pdl_cluster(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
                            dim3(tc::THREADS), tc::SMEM, s, P.cluster, tk, tv, P);
