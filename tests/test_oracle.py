@@ -427,6 +427,40 @@ def test_attention_against_torch_sdpa_float64():
         assert np.allclose(out[b], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
 
 
+def test_attention_prefill_from_empty_is_causal_sdpa():
+    """A whole sequence as new rows (L = M = 40, a prefill from an empty cache):
+    row m sees keys 0..m, which is the textbook causal attention
+    (scaled_dot_product_attention with is_causal=True, no hand-built mask)."""
+    case, kc, vc = _small_cache(115, [40], 40, ps=8, Hq=6, Hkv=2)
+    out = _run(case, kc, vc)
+    kd = oracle.e4m3_decode(kc) * 0.02
+    vd = oracle.e4m3_decode(vc) * 0.03
+    bt = case.layout.block_table.numpy()
+    keys = torch.from_numpy(np.stack([kd[bt[0, j // 8], :, j % 8] for j in range(40)], 1)).repeat_interleave(3, 0)
+    vals = torch.from_numpy(np.stack([vd[bt[0, j // 8], :, j % 8] for j in range(40)], 1)).repeat_interleave(3, 0)
+    qf = torch.from_numpy(case.q.float().numpy().astype(np.float64))[0].transpose(0, 1)   # [Hq][M][D]
+    ref = torch.nn.functional.scaled_dot_product_attention(qf, keys, vals, is_causal=True, scale=case.sm_scale)
+    assert np.allclose(out[0], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_prefill_chunk_constant_keys_running_mean():
+    """A chunk of M = 24 new rows at the end of L = 50 with every key equal:
+    row m (position 26 + m) returns the mean of the values it sees -- all
+    earlier positions (global) or the last W = 7 (window_left 6)."""
+    case, kc, vc = _small_cache(117, [50], 24, ps=4, window=7)
+    kc[:] = 0x3A
+    vd = oracle.e4m3_decode(vc) * 0.03
+    bt = case.layout.block_table.numpy()
+    for wl in (6, -1):
+        out = _run(case, kc, vc, window_left=wl)
+        for m in range(24):
+            p = 26 + m
+            lo = 0 if wl < 0 else max(0, p - wl)
+            for h in range(4):
+                vals = [vd[bt[0, j // 4], h // 2, j % 4] for j in range(lo, p + 1)]
+                assert np.allclose(out[0, m, h], np.mean(vals, axis=0), rtol=1e-12, atol=1e-15)
+
+
 def test_attention_bf16_cache_variant():
     case = gen.layer_case(121, [19], 2, 4, Hq=4, Hkv=2)
     P = case.layout.num_pages
