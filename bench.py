@@ -398,32 +398,48 @@ def _packed(tensors, device, align=256, pin=False):
     if pin:
         buf = buf.pin_memory()
     views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, tensors)]
-    return buf, views
+    return buf, views, offs
 
 
-def e2e_measure(w: Workload, steps, stream):
-    """Through the public API with host buffers: per step, one copy of every
-    layer's new tokens and queries from a pinned host buffer, the step's
-    calls, and one copy of every layer's attention output back into pinned
-    host memory (the layers read and write views of the two device staging
-    buffers).  The step is captured once in a CUDA graph (copies included)
-    and replayed, as a serving loop would run it; the same step launched
-    eagerly from Python is timed too (`eager_ms_per_step`: binding and launch
-    overhead included).  Returns the outputs' agreement with the device-timed
-    step's outputs (same inputs and cache, same kernels: bit-identical)."""
+def e2e_measure(w: Workload, steps, stream, chunks=8):
+    """Through the public API with host buffers: per step, every layer's new
+    tokens and queries come from a pinned host buffer and every layer's
+    attention output goes back into pinned host memory (the layers read and
+    write views of two device staging buffers).  The copies run on a copy
+    stream, overlapped with the kernels: the inputs in `chunks` copies of
+    consecutive layers' inputs, each layer group starting once its chunk has
+    landed, and each group's outputs copied back as soon as it finishes.  The
+    step is captured once in a CUDA graph (copies included) and replayed, as a
+    serving loop would run it; the same step launched eagerly from Python is
+    timed too (`eager_ms_per_step`: binding and launch overhead included).
+    Returns the outputs' agreement with the device-timed step's outputs (same
+    inputs and cache, same kernels: bit-identical)."""
     layers = w.copies[0]
     dev = layers[0].q.device
     names = [["q", "k_new", "v_new"] if l.fused is None else ["fq", "fk", "fv", "fpos", "fslots"] for l in layers]
     saved_in = [[getattr(l, n) for n in ns] for l, ns in zip(layers, names)]
     saved_out = [l.out for l in layers]
     flat_in = [t for ts in saved_in for t in ts]
-    dev_in, dviews = _packed(flat_in, dev)
-    host_in, hviews = _packed(flat_in, "cpu", pin=True)
+    dev_in, dviews, in_offs = _packed(flat_in, dev)
+    host_in, hviews, _ = _packed(flat_in, "cpu", pin=True)
     for h, t in zip(hviews, flat_in):
         h.copy_(t)
-    dev_out, oviews = _packed(saved_out, dev)
-    host_out, hoviews = _packed(saved_out, "cpu", pin=True)
+    dev_out, oviews, out_offs = _packed(saved_out, dev)
+    host_out, hoviews, _ = _packed(saved_out, "cpu", pin=True)
     h2d, d2h = host_in.numel(), host_out.numel()
+    # layer groups and the byte ranges of their inputs and outputs
+    n = len(layers)
+    chunks = max(1, min(chunks, n))
+    bounds = [round(c * n / chunks) for c in range(chunks + 1)]
+    first = [0]
+    for ns in names:
+        first.append(first[-1] + len(ns))
+    in_cut = [in_offs[first[g]] if g < n else h2d for g in bounds]
+    out_cut = [out_offs[g] if g < n else d2h for g in bounds]
+    cstream = torch.cuda.Stream(device=dev)
+    ev_fork, ev_join = torch.cuda.Event(), torch.cuda.Event()
+    ev_in = [torch.cuda.Event() for _ in range(chunks)]
+    ev_out = [torch.cuda.Event() for _ in range(chunks)]
     it = iter(dviews)
     for l, ns in zip(layers, names):
         for n in ns:
@@ -433,11 +449,23 @@ def e2e_measure(w: Workload, steps, stream):
     torch.cuda.synchronize()
 
     def one():
-        with torch.cuda.stream(stream):
-            dev_in.copy_(host_in, non_blocking=True)
-            for l in layers:
-                l.step(w.ws)
-            host_out.copy_(dev_out, non_blocking=True)
+        ev_fork.record(stream)
+        cstream.wait_event(ev_fork)
+        with torch.cuda.stream(cstream):
+            for c in range(chunks):
+                dev_in[in_cut[c]:in_cut[c + 1]].copy_(host_in[in_cut[c]:in_cut[c + 1]], non_blocking=True)
+                ev_in[c].record(cstream)
+        for c in range(chunks):
+            stream.wait_event(ev_in[c])
+            with torch.cuda.stream(stream):
+                for l in layers[bounds[c]:bounds[c + 1]]:
+                    l.step(w.ws)
+            ev_out[c].record(stream)
+            cstream.wait_event(ev_out[c])
+            with torch.cuda.stream(cstream):
+                host_out[out_cut[c]:out_cut[c + 1]].copy_(dev_out[out_cut[c]:out_cut[c + 1]], non_blocking=True)
+        ev_join.record(cstream)
+        stream.wait_event(ev_join)
 
     def timed(run, n):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -453,7 +481,8 @@ def e2e_measure(w: Workload, steps, stream):
         torch.cuda.synchronize()
         match = all(torch.equal(h, o.cpu()) for h, o in zip(hoviews, saved_out))
         eager_s = timed(one, steps)
-        mode = "step captured in a CUDA graph with one pinned-host copy in and one out, replayed"
+        mode = (f"step captured in a CUDA graph and replayed; pinned-host copies on a copy stream "
+                f"overlapped with the kernels ({chunks} input chunks, outputs per layer group)")
         try:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
