@@ -57,3 +57,30 @@ def test_reference_arm_only_rank0_prints():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_clock_samples_inside_the_load_window():
+    """The clock summary keeps the nvidia-smi samples taken while the measured
+    work ran (and all samples when none fell inside), with the throttle
+    reasons seen there."""
+    import datetime
+    import time
+    sys.path.insert(0, ROOT)
+    import bench
+    now = time.time()
+
+    def fmt(t):
+        return datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    c = bench.ClockSampler(0)
+    idle = "Not Active, Not Active, Not Active, Not Active"
+    capped = "Not Active, Not Active, Not Active, Active"
+    c.lines = [f"{fmt(now - 1)}, 0, 2070, 2070, 300.0, 0x0, {idle}",
+               f"{fmt(now + 0.1)}, 0, 1650, 2070, 1390.0, 0x4, {capped}",
+               f"{fmt(now + 0.2)}, 0, 1700, 2070, 1385.0, 0x4, {capped}",
+               f"{fmt(now + 2)}, 0, 2070, 2070, 300.0, 0x0, {idle}"]
+    c.load(now, now + 1)
+    s = c.summary()
+    assert (s["sm_mhz"], s["samples_under_load"], s["reasons"]) == (1675.0, 2, ["sw_power_cap"])
+    c.window = None
+    s = c.summary()
+    assert (s["samples"], s["samples_under_load"]) == (4, 0)
