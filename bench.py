@@ -261,13 +261,20 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
 # ------------------------------------------------------------------ timing
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 100 ms while the block runs; `load(t0, t1)`
+    marks the host-time window in which the GPU ran the measured work, and the
+    summary keeps the samples taken inside it (all samples when none is)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.window = None
+
+    def load(self, t0, t1):
+        self.window = (t0, t1)
 
     def __enter__(self):
         try:
@@ -291,24 +298,27 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        import datetime
         if not getattr(self, "lines", None):
             return None
-        sm, mx, reasons = [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in self.lines:
             f = [x.strip() for x in l.split(",")]
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(f[2]), float(f[3]), float(f[4]),
+                             [n for n, v in zip(names, f[6:10]) if v.lower().startswith("active")]))
+            except (ValueError, IndexError):
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [r for r in rows if self.window and self.window[0] <= r[0] <= self.window[1]]
+        use = inside or rows
+        reasons = sorted({n for r in use for n in r[4]})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in rows),
+                "power_w_max": max(r[3] for r in use), "reasons": reasons, "samples": len(use),
+                "samples_under_load": len(inside)}
 
 
 def time_graphs(graphs, steps, warmup, stream):
@@ -682,7 +692,18 @@ def main():
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        t_load = time.time()
         secs = time_graphs(graphs, args.steps, args.warmup, stream)
+        # the same replays continue untimed until the load has lasted 1 s, so
+        # that the 100 ms clock samples see it even when the timed steps are few
+        n_soak = 0
+        while time.time() - t_load < 1.0 and n_soak < 100000:
+            with torch.cuda.stream(stream):
+                for g in graphs:
+                    g.replay()
+            n_soak += len(graphs)
+            torch.cuda.synchronize()
+        clk.load(t_load, time.time())
     barrier(ws)
     torch.cuda.synchronize()
     secs = max_over_ranks(secs, ws)
