@@ -169,8 +169,8 @@ size_t fp8kv_paged_attention_workspace_size(int B, int M, int Hq, int Hkv, int D
  * computed with fp32 accumulation.  Long contexts are cut into partitions of
  * split_tokens keys whose partial (max, sum, unnormalised output) are combined
  * through their log-sum-exp: by a reduce kernel over workspace partials, or,
- * for one sequence (B = 1) of 17 to 128 rows per KV head on an E4M3 cache in
- * at most 8 partitions, on chip by the partitions of a KV head running as one
+ * for one sequence (B = 1) of 17 to 128 rows per KV head (one row tile) on an
+ * E4M3 cache in at most 8 partitions, on chip by the partitions of a KV head running as one
  * thread-block cluster (fp8kv_last_dispatch reports "cluster=N").
  *
  *   q            (device) bf16 [B][M][Hq][D]

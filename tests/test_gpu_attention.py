@@ -365,6 +365,21 @@ def test_prefill_append_equals_insert_then_attention():
     assert_close(out, oracle_attention(case, okc, ovc), "prefill append")
 
 
+@pytest.mark.parametrize("M,window", [(12, None), (12, 512), (1, None)])
+def test_unit_scale_draft_cache_layer(M, window):
+    """The draft model's cache layers hold E4M3 with K/V scales of exactly 1.0
+    (no calibration): the codes are the bf16 values rounded onto the E4M3
+    grid as they are (bit-exact against the oracle), and attention over them
+    stays within tolerance."""
+    case = gen.layer_case(9800 + M + (window or 0), [700, 260], M, 32, window=window)
+    case = gen.LayerCase(**{**case.__dict__, "k_scale": 1.0, "v_scale": 1.0})
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    out = gpu_attention(case, kc, vc, ks, vs)
+    assert_close(out, oracle_attention(case, okc, ovc), f"unit scale M={M} window={window}")
+
+
 # ------------------------------------------------------------ the configs
 
 def test_cfg1_tiny_decode():

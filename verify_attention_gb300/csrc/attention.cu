@@ -27,7 +27,10 @@
 //    memory at the end;
 //  * one partition per sequence writes bf16 output directly; otherwise each
 //    partition writes (max, sum, unnormalised output) and attn_reduce_kernel
-//    combines them.
+//    combines them (per row, over the partitions of that row's tile).
+// More than 16 rows per KV head on an E4M3 cache go to the tcgen05 kernel
+// (attention_tc.cu); this file also holds the plan, the reduce kernel and
+// the C-ABI entry points.
 #include <stdio.h>
 
 #include "attention.cuh"
