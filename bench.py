@@ -214,6 +214,25 @@ def _free_context(cases):
     torch.cuda.empty_cache()
 
 
+def workload_page_size(name, page_size_arg):
+    """The page size a workload runs at (the verify step takes --page-size)."""
+    return page_size_arg if name == "verify48" else (64 if name in ("decode128k", "prefill16k") else 32)
+
+
+def workload_description(name, page_size, cache_dtype="e4m3"):
+    return {
+        "verify48": (f"48 layers [SW512,SW512,SW512,G]x12, B=1, M=12, Hq=72, Hkv=8, D=128, L=8192, "
+                     f"page {page_size}, E4M3 cache; per layer 12-token insert + attention"),
+        "decode128k": (f"12 global layers, B=1, M=1, Hq=72, Hkv=8, D=128, L=131072, page 64, "
+                       f"{cache_dtype} cache; per layer 1-token insert + split-KV attention + reduce"),
+        "prefill16k": ("4 global layers, B=1, a prefill chunk of M=1024 tokens at the end of L=16384, Hq=72, "
+                       "Hkv=8, D=128, page 64, E4M3 cache; per layer 1024-token append + causal attention in "
+                       "128-row tiles"),
+        "serving64": ("8 layers G/SW512 alternating, B=64, L~U[1024,32768] (seed 1005), M=12, Hq=72, Hkv=8, "
+                      "D=128, page 32, E4M3 cache; per layer fused Q/K RMSNorm+RoPE+insert + attention"),
+    }[name]
+
+
 def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
     if name == "verify48":
         n = layers or 48
@@ -222,27 +241,21 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
         ncopies = max(2, math.ceil(4 * L2_BYTES / per_copy))
         copies = [[Layer(c, device) for c in base] for _ in range(ncopies)]
         _free_context(base)
-        desc = (f"48 layers [SW512,SW512,SW512,G]x12, B=1, M=12, Hq=72, Hkv=8, D=128, L=8192, "
-                f"page {page_size}, E4M3 cache; per layer 12-token insert + attention")
-        return Workload(name, copies, desc, 12)
+        return Workload(name, copies, workload_description(name, page_size), 12)
     if name == "decode128k":
         copies = [[]]
         for l in range(layers or 12):
             c = gen.cfg4_case(l, device=device)
             copies[0].append(Layer(c, device, cache_dtype=cache_dtype, split_tokens=0))
             _free_context([c])
-        desc = (f"12 global layers, B=1, M=1, Hq=72, Hkv=8, D=128, L=131072, page 64, "
-                f"{cache_dtype} cache; per layer 1-token insert + split-KV attention + reduce")
-        return Workload(name, copies, desc, 1)
+        return Workload(name, copies, workload_description(name, 64, cache_dtype), 1)
     if name == "prefill16k":
         copies = [[]]
         for l in range(layers or 4):
             c = gen.layer_case(1006 * 100 + l, [16384], 1024, 64, window=None, device=device)
             copies[0].append(Layer(c, device, split_tokens=0))
             _free_context([c])
-        desc = ("4 global layers, B=1, a prefill chunk of M=1024 tokens at the end of L=16384, Hq=72, Hkv=8, "
-                "D=128, page 64, E4M3 cache; per layer 1024-token append + causal attention in 128-row tiles")
-        return Workload(name, copies, desc, 1024)
+        return Workload(name, copies, workload_description(name, 64), 1024)
     if name == "serving64":
         lens = gen.cfg5_seq_lens()
         built = []
@@ -251,10 +264,7 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
             f = gen.fused_case(1005 * 100 + 50 + l, c.layout, 12)
             built.append(Layer(c, device, fused=f))
             _free_context([c])
-        layers = built
-        desc = ("8 layers G/SW512 alternating, B=64, L~U[1024,32768] (seed 1005), M=12, Hq=72, Hkv=8, "
-                "D=128, page 32, E4M3 cache; per layer fused Q/K RMSNorm+RoPE+insert + attention")
-        return Workload(name, [built], desc, 64 * 12)
+        return Workload(name, [built], workload_description(name, 32), 64 * 12)
     raise ValueError(name)
 
 
@@ -634,7 +644,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    sample = OracleSample(args.workload, args.page_size)
+    ps = workload_page_size(args.workload, args.page_size)
+    sample = OracleSample(args.workload, ps)
     _, t1 = sample.run(1)
     budget = 150.0 / (args.warmup + args.steps)          # seconds of oracle work per step
     n = int(min(len(sample.rows_all), max(1, budget / max(t1, 1e-4))))
@@ -649,7 +660,9 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": args.workload, "page_size": args.page_size},
+            "data": "synthetic", "config": {"workload": args.workload,
+                                            "description": workload_description(args.workload, ps),
+                                            "page_size": ps},
             "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": desc + f"; host has {os.cpu_count()} cores"},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -683,8 +696,7 @@ def main():
     stream = torch.cuda.Stream(device=dev)
     hbm_peak, bf16_peak, peak_src = peaks()
 
-    ps = args.page_size if args.workload == "verify48" else (64 if args.workload in ("decode128k", "prefill16k")
-                                                             else 32)
+    ps = workload_page_size(args.workload, args.page_size)
     w = build_workload(args.workload, ps, dev, layers=args.layers)
     graphs, launches_per_step = capture_step_graphs(w, stream)
     fp8kv.fp8kv_device_status(clear=True)
