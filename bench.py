@@ -192,6 +192,7 @@ class Workload:
         self.copies = layers_per_copy           # [copy][layer]
         self.description = description
         self.unit_rows = unit_rows
+        self.inputs_sha256 = None               # of the first layer's generated inputs
         dev = layers_per_copy[0][0].q.device
         need = max(l.ws_bytes for c in layers_per_copy for l in c)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
@@ -205,6 +206,21 @@ class Workload:
 
     def flops_per_step(self):
         return sum(l.flops() for l in self.copies[0])
+
+
+def case_sha256(case):
+    """SHA-256 of one layer's generated inputs (queries, context and new
+    K/V, slots, block table, sequence lengths): a fingerprint of the inputs."""
+    import hashlib
+    h = hashlib.sha256()
+    try:
+        for t in (case.q, case.k_prior, case.v_prior, case.k_new, case.v_new, case.slots_prior, case.slots_new,
+                  case.layout.block_table, case.layout.seq_lens):
+            if t is not None:
+                h.update(t.detach().contiguous().cpu().view(torch.uint8).numpy().tobytes())
+    except (RuntimeError, TypeError) as e:     # a fingerprint is extra: never stop the measurement
+        return f"unavailable: {str(e)[:80]}"
+    return h.hexdigest()
 
 
 def _free_context(cases):
@@ -233,6 +249,11 @@ def workload_description(name, page_size, cache_dtype="e4m3"):
     }[name]
 
 
+def _fingerprinted(w, sha):
+    w.inputs_sha256 = sha
+    return w
+
+
 def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
     if name == "verify48":
         n = layers or 48
@@ -240,22 +261,25 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
         per_copy = sum(bm.attention_bytes([8192], 12, 72, 8, 128, 1, -1, page_size) for _ in range(n))
         ncopies = max(2, math.ceil(4 * L2_BYTES / per_copy))
         copies = [[Layer(c, device) for c in base] for _ in range(ncopies)]
+        fp = case_sha256(base[0])
         _free_context(base)
-        return Workload(name, copies, workload_description(name, page_size), 12)
+        return _fingerprinted(Workload(name, copies, workload_description(name, page_size), 12), fp)
     if name == "decode128k":
         copies = [[]]
         for l in range(layers or 12):
             c = gen.cfg4_case(l, device=device)
             copies[0].append(Layer(c, device, cache_dtype=cache_dtype, split_tokens=0))
+            fp = case_sha256(c) if l == 0 else fp
             _free_context([c])
-        return Workload(name, copies, workload_description(name, 64, cache_dtype), 1)
+        return _fingerprinted(Workload(name, copies, workload_description(name, 64, cache_dtype), 1), fp)
     if name == "prefill16k":
         copies = [[]]
         for l in range(layers or 4):
             c = gen.layer_case(1006 * 100 + l, [16384], 1024, 64, window=None, device=device)
             copies[0].append(Layer(c, device, split_tokens=0))
+            fp = case_sha256(c) if l == 0 else fp
             _free_context([c])
-        return Workload(name, copies, workload_description(name, 64), 1024)
+        return _fingerprinted(Workload(name, copies, workload_description(name, 64), 1024), fp)
     if name == "serving64":
         lens = gen.cfg5_seq_lens()
         built = []
@@ -263,8 +287,9 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
             c = gen.cfg5_case(l, device=device, seq_lens=lens)
             f = gen.fused_case(1005 * 100 + 50 + l, c.layout, 12)
             built.append(Layer(c, device, fused=f))
+            fp = case_sha256(c) if l == 0 else fp
             _free_context([c])
-        return Workload(name, [built], workload_description(name, 32), 64 * 12)
+        return _fingerprinted(Workload(name, [built], workload_description(name, 32), 64 * 12), fp)
     raise ValueError(name)
 
 
@@ -344,6 +369,21 @@ def time_graphs(graphs, steps, warmup, stream):
         end.record(stream)
     end.synchronize()
     return start.elapsed_time(end) / 1e3
+
+
+def step_percentiles(graphs, n, stream):
+    """Device time of each of n further replays (an event between every two),
+    outside the timed region: p10, p50, p90 in ms."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(n):
+            graphs[i % len(graphs)].replay()
+            evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    d = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(n))
+    return {"p10": d[int(0.1 * (n - 1))], "p50": d[int(0.5 * (n - 1))], "p90": d[int(0.9 * (n - 1))],
+            "steps": n}
 
 
 def capture_step_graphs(w: Workload, stream):
@@ -723,6 +763,10 @@ def main():
     if status:
         raise RuntimeError(f"device status {status:#x} after the timed region")
 
+    try:
+        pct = step_percentiles(graphs, max(10, min(args.steps, 200)), stream)
+    except Exception as e:                       # a distribution is extra; the timed mean stands
+        pct = {"error": str(e)[:120]}
     step_bytes = w.bytes_per_step()
     step_s = secs / args.steps
     value = whole_job_gbs(ws, step_bytes, step_s)
@@ -734,11 +778,13 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "step_ms_percentiles": pct,
+        "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3 cache, f16/fp32 math", "data": "synthetic",
         "config": {"workload": args.workload, "description": w.description, "page_size": ps,
                    "cache_copies": len(w.copies), "l2": "inputs larger than L2: cache copies rotate",
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "first_layer_inputs_sha256": w.inputs_sha256},
         "verify_steps_per_s": ws / step_s,
         "pct_of_hbm_roofline": value / ws / hbm_peak,
         "algorithmic_bytes_per_step": step_bytes,
