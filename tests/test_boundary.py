@@ -169,6 +169,34 @@ def test_automatic_plans(L):
     assert plan(64, 12, 72, 8, 128, 32, 32768, -1, 0) == (4, 8192)   # batch: a quarter of 32768
 
 
+def test_plan_invariants_over_many_shapes(L):
+    """For seeded random shapes, explicit and automatic plans: whole pages per
+    partition, enough partitions to cover every visible key, whole 128-key
+    tiles for automatic plans (the tcgen05 kernel needs them above 16 rows per
+    KV head), and a workspace exactly when a sequence spans partitions."""
+    import random
+    rng = random.Random(5)
+    for _ in range(400):
+        ps = rng.choice([32, 64])
+        Hkv = rng.choice([1, 2, 8])
+        G = rng.choice([1, 4, 9])
+        M = rng.choice([1, 3, 12, 16, 40, 300, 1024])
+        B = rng.choice([1, 3, 64])
+        msl = rng.randint(M, 40000)
+        wl = rng.choice([-1, 0, 63, 511])
+        split = rng.choice([0, 0, ps, 4 * ps, 2048])
+        ns, st = fp8kv.fp8kv_paged_attention_plan(B, M, G * Hkv, Hkv, 128, ps, msl, wl, split)
+        assert ns >= 1 and st > 0 and st % ps == 0
+        pages = -(-msl // ps)
+        if wl >= 0:
+            pages = min(pages, -(-(M + wl) // ps) + 1)
+        assert ns * (st // ps) >= pages and (ns - 1) * (st // ps) < pages
+        if split == 0:
+            assert st % 128 == 0
+        ws = fp8kv.fp8kv_paged_attention_workspace_size(B, M, G * Hkv, Hkv, 128, ps, msl, wl, split)
+        assert ws == (0 if ns == 1 else B * M * G * Hkv * ns * 130 * 4)
+
+
 def test_binding_rejects_cpu_tensors():
     k = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
