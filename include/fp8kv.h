@@ -247,12 +247,17 @@ int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const voi
  * library routine).
  *
  * Arguments and results are those of fp8kv_paged_attention without
- * workspace / workspace_bytes.  Requests whose workspace size
- * (fp8kv_paged_attention_workspace_size) exceeds 32 MiB return
+ * workspace / workspace_bytes; out must hold B*M*Hq*D bf16 values (the C
+ * entry point cannot check its size).  Every argument is validated first,
+ * with the statuses of fp8kv_paged_attention; then a request whose workspace
+ * size (fp8kv_paged_attention_workspace_size) exceeds 32 MiB returns
  * FP8KV_ERR_WORKSPACE (a larger split_tokens needs less; otherwise use the
- * allocating entry point).  The first call on a device looks up the buffer's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call shares the one buffer, which keeps
+ * allocating entry point).  The first call on a device looks up the buffer's
+ * device address (cudaGetSymbolAddress, with that device current) and keeps
+ * it for the life of the process; make that first call before any stream
+ * capture.  A cudaDeviceReset while the library is loaded is not supported
+ * (the kept address, like the kernels' shared-memory opt-ins, would be
+ * stale).  Every call shares the one buffer, which keeps
  * the last call's contents (no part of it needs to start at zero): calls
  * that overlap on the GPU -- on different streams, or from several threads --
  * race and must be serialised by the caller.
@@ -271,6 +276,20 @@ int fp8kv_paged_attention_noalloc(const void* q, const void* k_cache, const void
  * of the encoder).  out (device) uint8 [n].
  */
 int fp8kv_e4m3_encode_bits(uint32_t first, size_t n, uint8_t* out, void* stream);
+
+/*
+ * fp8kv_selftest_bounded_wait -- exercise the device-side failure path of a
+ * pipeline wait: one warp waits on a barrier that by construction gets no
+ * arrival; after limit_us microseconds (1 .. 2000000) the wait gives up, sets
+ * FP8KV_DEV_WAIT_TIMEOUT in the device status word and the kernel returns, so
+ * the context stays usable.  Every barrier wait of the attention kernels takes
+ * the same path after 2 s.  ("Laguna S 2.1 B70 campaign transfer ledger",
+ * section "Harness, recovery, and evidence lessons": a stage that does not
+ * finish is classified from a bounded wait and a recorded marker, never left
+ * to hang.)  Returns FP8KV_OK when launched; read the bit with
+ * fp8kv_device_status().
+ */
+int fp8kv_selftest_bounded_wait(unsigned int limit_us, void* stream);
 
 /* Text of a status code (static storage). */
 const char* fp8kv_status_string(int status);

@@ -40,6 +40,11 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_selftest_limit_validation_needs_no_device(L):
+    assert L.fp8kv_selftest_bounded_wait(0, NULL) == 1
+    assert L.fp8kv_selftest_bounded_wait(2000001, NULL) == 1
+
+
 def test_status_strings(L):
     assert fp8kv.fp8kv_status_string(0) == "ok"
     assert "unsupported" in fp8kv.fp8kv_status_string(2)

@@ -63,6 +63,25 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
 
 
 @pytest.mark.gpu
+def test_noalloc_single_sequence_cluster_path():
+    """One sequence of verifier rows in at most 8 partitions: the partitions of
+    a KV head combine on chip as a thread-block cluster.  The call still gets
+    the shared buffer's address (the workspace is reserved for that shape), so
+    it runs through the allocation-free entry point too, twice in a row."""
+    f = _lib()
+    f.fp8kv_device_status(clear=True)
+    case = gen.layer_case(9103, [1000], 12, 32)                   # 8 tiles of 128 keys
+    kc, vc, ks, vs = gpu_caches(case)
+    ref = gpu_attention(case, kc, vc, ks, vs)
+    assert "cluster=8 " in f.fp8kv_last_dispatch()
+    for _ in range(2):
+        got = _noalloc(f, case, kc, vc, ks, vs, 0)
+        assert "cluster=8 " in f.fp8kv_last_dispatch()
+        _close(got, ref)
+    assert f.fp8kv_device_status(clear=True) == 0
+
+
+@pytest.mark.gpu
 def test_noalloc_rejects_requests_beyond_its_buffer():
     f = _lib()
     L = f.lib()
@@ -73,3 +92,15 @@ def test_noalloc_rejects_requests_beyond_its_buffer():
     rc = L.fp8kv_paged_attention_noalloc(p, p, p, 0, p, 1024, p, 32768, 64, 12, 72, 8, 128, 32, 70000, p, p,
                                          0.088, -1, 256, p, None)
     assert rc == 3   # FP8KV_ERR_WORKSPACE, nothing launched
+    # an invalid request that is also too large reports the invalid argument
+    rc = L.fp8kv_paged_attention_noalloc(None, p, p, 0, p, 1024, p, 32768, 64, 12, 72, 8, 128, 32, 70000, p, p,
+                                         0.088, -1, 256, p, None)
+    assert rc == 1   # FP8KV_ERR_INVALID_ARG
+    # the binding refuses an output buffer smaller than q
+    case = gen.layer_case(9104, [300], 12, 32)
+    kc, vc, ks, vs = gpu_caches(case)
+    lay = case.layout
+    with pytest.raises(ValueError):
+        f.fp8kv_paged_attention_noalloc(case.q.cuda(), kc, vc, lay.block_table.cuda(), lay.seq_lens.cuda(), 300,
+                                        ks, vs, case.sm_scale, torch.empty(1, 12, 72, 64, dtype=torch.bfloat16,
+                                                                           device="cuda"))

@@ -44,21 +44,13 @@ constexpr int kMaxRowTiles = 9;          // M*G <= 144 on the mma.sync kernels
 constexpr int kMaxM = 16384;             // query rows per sequence (prefill chunks; E4M3 cache)
 // Bytes of K/V stages per CTA for several row tiles; for the decode shape
 // (one row tile) the key groups, their stage budget and the register cap of
-// the decode kernel.  Overridable at build time for tuning sweeps.
-#ifndef FP8KV_STAGE_KB
-#define FP8KV_STAGE_KB 96
-#endif
-#ifndef FP8KV_DECODE_KEY_GROUPS
-#define FP8KV_DECODE_KEY_GROUPS 7
-#endif
-#ifndef FP8KV_DECODE_STAGE_KB
-#define FP8KV_DECODE_STAGE_KB 224
-#endif
-#ifndef FP8KV_DECODE_REGS
-#define FP8KV_DECODE_REGS 200
-#endif
-constexpr int kStageBudget = FP8KV_STAGE_KB * 1024;
-constexpr int kDecodeStageBudget = FP8KV_DECODE_STAGE_KB * 1024;
+// the decode kernel.  Chosen by graph-timed sweeps on a 131072-token decode
+// layer (key groups x stages, one CTA per SM): 4 x 1 at two CTAs per SM
+// 4.24 TB/s, 4 x 3: 4.08, 5 x 2: 4.04, 6 x 2: 4.66, 7 x 2: 4.80.
+constexpr int kStageBudget = 96 * 1024;
+constexpr int kDecodeKeyGroups = 7;
+constexpr int kDecodeStageBudget = 224 * 1024;
+constexpr int kDecodeRegs = 200;
 
 template <int PS, bool FP8>
 struct Cfg {
@@ -525,7 +517,7 @@ __global__ void __launch_bounds__(32 * (kMaxRowTiles + 1), 1) paged_attention_ke
 // stages in flight, one CTA per SM; at most two warps per SM sub-partition,
 // so the register cap can be high enough to keep every fragment resident.
 template <int PS, bool FP8>
-__global__ void __maxnreg__(FP8KV_DECODE_REGS) paged_decode_kernel(
+__global__ void __maxnreg__(kDecodeRegs) paged_decode_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, AttnParams P) {
     attention_body<PS, FP8>(tm_k, tm_v, P);
 }
@@ -856,7 +848,7 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
                                            : (fp8 ? Cfg<64, true>::kStages : Cfg<64, false>::kStages);
         const int elem_b = fp8 ? 1 : 2;
         const int dstages = kDecodeStageBudget / (2 * page_size * 128 * elem_b);
-        int kw = P.NT == 1 ? FP8KV_DECODE_KEY_GROUPS : (P.NT == 2 ? 2 : 1);
+        int kw = P.NT == 1 ? kDecodeKeyGroups : (P.NT == 2 ? 2 : 1);
         const int avail = P.NT == 1 ? dstages : stages;
         kw = std::max(1, std::min(kw, avail));
         int sg = std::max(1, avail / kw);
@@ -989,13 +981,14 @@ extern "C" int fp8kv_paged_attention_noalloc(const void* q, const void* k_cache,
                                              int split_tokens, void* out, void* stream) {
     const size_t need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len,
                                                              window_left, split_tokens);
-    if (need == (size_t)-1) {
-        // same validation and status as the allocating entry point
+    if (need == (size_t)-1 || need > FP8KV_NOALLOC_WORKSPACE_BYTES) {
+        // the allocating entry point without a workspace: every argument check
+        // runs first (same statuses), then a request that needs workspace
+        // partials returns FP8KV_ERR_WORKSPACE; nothing is launched either way
         return fp8kv_paged_attention(q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq, seq_lens,
                                      max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale,
                                      sm_scale, window_left, split_tokens, nullptr, 0, out, stream);
     }
-    if (need > FP8KV_NOALLOC_WORKSPACE_BYTES) return FP8KV_ERR_WORKSPACE;
     void* ws = nullptr;
     if (need) {
         const int rc = noalloc_workspace(&ws);

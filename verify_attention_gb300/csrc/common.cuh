@@ -172,9 +172,10 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 
 // Wait for the phase with parity `phase` of an mbarrier to complete.  Gives up
-// after ~2 s of wall time (sets FP8KV_DEV_WAIT_TIMEOUT and returns false) so a
-// broken pipeline can never hang the GPU.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
+// after `limit_ns` of wall time (2 s unless a caller asks otherwise; sets
+// FP8KV_DEV_WAIT_TIMEOUT and returns false) so a broken pipeline can never
+// hang the GPU.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t limit_ns = 2000000000ull) {
     uint32_t ok;
     asm volatile(
         "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
@@ -191,7 +192,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
             : "r"(bar), "r"(phase), "r"(500000u)
             : "memory");
         if (ok) return true;
-        if (globaltimer() - start > 2000000000ull) {
+        if (globaltimer() - start > limit_ns) {
             flag(FP8KV_DEV_WAIT_TIMEOUT);
             return false;
         }

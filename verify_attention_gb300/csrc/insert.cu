@@ -222,9 +222,32 @@ __global__ void __launch_bounds__(256) encode_bits_kernel(uint32_t first, uint64
     }
 }
 
+// ------------------------------------------------ bounded-wait self-test
+
+// One warp waits on an mbarrier that nothing ever arrives on: the wait gives
+// up after limit_ns, sets FP8KV_DEV_WAIT_TIMEOUT and the kernel returns like
+// any pipeline kernel whose wait ran out (no trap, the context stays usable).
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, limit_ns);
+    __syncwarp();
+}
+
 }  // namespace fp8kv
 
 using namespace fp8kv;
+
+extern "C" int fp8kv_selftest_bounded_wait(unsigned int limit_us, void* stream) {
+    if (limit_us == 0 || limit_us > 2000000u) return FP8KV_ERR_INVALID_ARG;
+    bounded_wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_us * 1000ull);
+    count_launch();
+    return launch_status();
+}
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 

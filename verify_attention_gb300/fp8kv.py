@@ -58,6 +58,8 @@ def lib() -> ctypes.CDLL:
                                                     i32, i32, i32, vp, vp, f32, i32, i32, vp, vp]
         L.fp8kv_e4m3_encode_bits.restype = i32
         L.fp8kv_e4m3_encode_bits.argtypes = [u32, sz, vp, vp]
+        L.fp8kv_selftest_bounded_wait.restype = i32
+        L.fp8kv_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
         L.fp8kv_status_string.restype = ctypes.c_char_p
         L.fp8kv_status_string.argtypes = [i32]
         L.fp8kv_last_dispatch.restype = i32
@@ -225,6 +227,8 @@ def fp8kv_paged_attention_noalloc(q, k_cache, v_cache, block_table, seq_lens, ma
     _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
     _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
     _dev(out, "out", torch.bfloat16)
+    if out.shape != q.shape or out.device != q.device:
+        raise ValueError(f"out must have the shape and device of q {tuple(q.shape)}, got {tuple(out.shape)}")
     B, M, Hq, D = q.shape
     P, Hkv, page_size, _ = k_cache.shape
     rc = lib().fp8kv_paged_attention_noalloc(
@@ -240,6 +244,12 @@ def fp8kv_e4m3_encode_bits(first: int, n: int, out: torch.Tensor, stream=None):
     _dev(out, "out", torch.uint8)
     rc = lib().fp8kv_e4m3_encode_bits(first, n, _ptr(out), _stream(stream))
     _check("fp8kv_e4m3_encode_bits", rc)
+
+
+def fp8kv_selftest_bounded_wait(limit_us: int, stream=None):
+    """Launch the kernel whose barrier wait runs out after limit_us (sets
+    DEV_WAIT_TIMEOUT in the device status word)."""
+    _check("fp8kv_selftest_bounded_wait", lib().fp8kv_selftest_bounded_wait(int(limit_us), _stream(stream)))
 
 
 def fp8kv_last_dispatch() -> str:
