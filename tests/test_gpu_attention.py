@@ -6,8 +6,7 @@ import torch
 
 import oracle
 from verify_attention_gb300 import build, inputs as gen
-from tests.helpers import (assert_close, gpu_attention, gpu_caches, oracle_attention, oracle_caches,
-                           sample_rows)
+from tests.helpers import assert_close, gpu_attention, gpu_caches, oracle_attention, oracle_caches
 
 pytestmark = pytest.mark.gpu
 
@@ -26,13 +25,13 @@ def fp8kv():
     return f
 
 
-def run_case(case, split_tokens=0, cache_dtype="e4m3", poison=0xA5, rows=None):
+def run_case(case, split_tokens=0, cache_dtype="e4m3", poison=0xA5, rows=None, impl="c"):
     kc, vc, ks, vs = gpu_caches(case, cache_dtype, poison=poison)
     out = gpu_attention(case, kc, vc, ks, vs, split_tokens=split_tokens)
     torch.cuda.synchronize()
     okc, ovc = oracle_caches(case, cache_dtype, poison=poison)
     if rows is None:
-        ref = oracle_attention(case, okc, ovc, cache_dtype=cache_dtype)
+        ref = oracle_attention(case, okc, ovc, cache_dtype=cache_dtype, impl=impl)
         return out, ref, assert_close(out, ref, f"split={split_tokens}")
     ref = oracle_attention(case, okc, ovc, rows=rows, cache_dtype=cache_dtype)
     o = out.float().cpu().numpy()[rows[:, 0], rows[:, 1], rows[:, 2]]
@@ -381,37 +380,123 @@ def test_unit_scale_draft_cache_layer(M, window):
 
 
 # ------------------------------------------------------------ the configs
+#
+# The five workloads at their full sizes.  Where the bench runs a layer
+# through the one-call append entry (new tokens into the cache, then
+# attention, automatic partitions), so does the test; every output row is
+# compared with the oracle (the float64 numpy implementation where the C loops
+# would take minutes), except on the serving mix, which is checked on every row
+# of 8 whole sequences and of one KV head of each other sequence per layer.
+
+
+def run_append_case(case, split_tokens=0, cache_dtype="e4m3", impl="numpy"):
+    """Context inserted, then fp8kv_append_paged_attention of the new tokens:
+    cache bytes bit-exact against the oracle's insert of every token, every
+    output row within tolerance of the oracle."""
+    f = fp8kv()
+    kc, vc, ks, vs = gpu_caches(case, cache_dtype, new_tokens=False)
+    lay = case.layout
+    B, M = case.q.shape[0], case.M
+    Hkv = case.k_new.shape[1]
+    out = f.fp8kv_append_paged_attention(case.k_new.cuda().view(B, M, Hkv, 128), case.v_new.cuda().view(B, M, Hkv, 128),
+                                         case.q.cuda(), kc, vc, lay.block_table.cuda(), lay.seq_lens.cuda(),
+                                         int(lay.seq_lens.max()), ks, vs, case.sm_scale,
+                                         window_left=case.window_left, split_tokens=split_tokens)
+    torch.cuda.synchronize()
+    okc, ovc = oracle_caches(case, cache_dtype)
+    if cache_dtype == "bf16":
+        gk, gv = gen.bf16_bits(kc), gen.bf16_bits(vc)
+    else:
+        gk, gv = kc.cpu().numpy(), vc.cpu().numpy()
+    assert np.array_equal(gk, okc) and np.array_equal(gv, ovc)
+    ref = oracle_attention(case, okc, ovc, cache_dtype=cache_dtype, impl=impl)
+    return out, ref, assert_close(out, ref, f"append split={split_tokens}")
+
 
 def test_cfg1_tiny_decode():
     run_case(gen.cfg1_case())
+    run_append_case(gen.cfg1_case(), impl="c")
 
 
 @pytest.mark.parametrize("window", [None, 512])
 def test_cfg2_single_layer_verify(window):
     run_case(gen.cfg2_case(window))
+    run_append_case(gen.cfg2_case(window))
 
 
 @pytest.mark.parametrize("ps", [32, 64])
 @pytest.mark.parametrize("layer", [0, 3])        # sliding, global
 def test_cfg3_verify_layers(layer, ps):
-    case = gen.cfg3_case(layer, ps)
-    rows = None if layer == 0 else sample_rows(1, 12, 72, 96, seed=layer)
-    run_case(case, rows=rows)
+    """A sliding and a global layer of the 48-layer step at both page sizes:
+    every one of the 864 output rows, through the append entry the bench
+    times (automatic partitions: a 5-CTA cluster on the sliding layer, 16
+    partitions and the reduce kernel on the global one)."""
+    run_append_case(gen.cfg3_case(layer, ps))
 
 
 @pytest.mark.parametrize("split_tokens", [2048, 0])
 def test_cfg4_long_context_decode_full_size(split_tokens):
     case = gen.cfg4_case(0)
-    run_case(case, split_tokens=split_tokens)
+    run_case(case, split_tokens=split_tokens, impl="numpy")
+    if split_tokens == 0:
+        run_append_case(case)
 
 
 def test_cfg4_bf16_cache_full_size():
-    case = gen.cfg4_case(1)
-    run_case(case, split_tokens=2048, cache_dtype="bf16", rows=sample_rows(1, 1, 72, 24, seed=4))
+    run_case(gen.cfg4_case(1), split_tokens=2048, cache_dtype="bf16", impl="numpy")
+    run_append_case(gen.cfg4_case(1), cache_dtype="bf16")
 
 
-@pytest.mark.parametrize("layer", [0, 1])        # global, sliding
-def test_cfg5_serving_mix_full_size_sampled(layer):
-    case = gen.cfg5_case(layer)
-    rows = sample_rows(64, 12, 72, 48, seed=layer)
-    run_case(case, rows=rows)
+def cfg5_subset(layer, lens, full_count=8, Hkv=8):
+    """The serving mix's checked rows on one layer: every KV head of 8 seeded
+    whole sequences (the shortest and the longest always among them), and one
+    seeded KV head of every other sequence."""
+    rng = np.random.default_rng(5000 + layer)
+    order = np.argsort(lens)
+    full = {int(order[0]), int(order[-1])}
+    for b in rng.permutation(len(lens)):
+        if len(full) == full_count:
+            break
+        full.add(int(b))
+    groups = [(b, hk) for b in sorted(full) for hk in range(Hkv)]
+    groups += [(b, int(rng.integers(Hkv))) for b in range(len(lens)) if b not in full]
+    return groups
+
+
+@pytest.mark.parametrize("layer", range(8))      # G, SW, G, SW, ...
+def test_cfg5_serving_mix_full_size(layer):
+    """Config 5 as the bench runs it, on every layer: 64 sequences of 1024 to
+    32768 tokens in one shared page-32 pool, the 12 new tokens of each through
+    the fused Q/K RMSNorm + RoPE + E4M3 insert, then attention over the normed,
+    rotated queries (automatic partitions).  Q and the whole cache bit-exact;
+    attention on the rows of cfg5_subset."""
+    import oracle
+    from oracle import attention_np
+    f = fp8kv()
+    lens = gen.cfg5_seq_lens()
+    case = gen.cfg5_case(layer, device="cuda", seq_lens=lens)
+    fc = gen.fused_case(1005 * 100 + 50 + layer, case.layout, 12)
+    lay = case.layout
+    kc, vc, ks, vs = gpu_caches(case, new_tokens=False)
+    q_out = torch.empty(fc.q.shape, dtype=torch.bfloat16, device="cuda")
+    f.fp8kv_qk_norm_rope_insert(fc.q.cuda(), fc.k.cuda(), fc.v.cuda(), fc.positions.cuda(), fc.q_norm_w.cuda(),
+                                fc.k_norm_w.cuda(), fc.eps, fc.cos_sin.cuda(), q_out, fc.slots.cuda(), ks, vs, kc, vc)
+    q = q_out.view(len(lens), 12, 72, 128)
+    out = f.fp8kv_paged_attention(q, kc, vc, lay.block_table.cuda(), lay.seq_lens.cuda(), max(lens), ks, vs,
+                                  case.sm_scale, window_left=case.window_left)
+    torch.cuda.synchronize()
+    okc, ovc = oracle_caches(case, new_tokens=False)
+    oq = oracle.qk_norm_rope_insert(gen.bf16_bits(fc.q), gen.bf16_bits(fc.k), gen.bf16_bits(fc.v),
+                                    fc.positions.numpy(), gen.bf16_bits(fc.q_norm_w), gen.bf16_bits(fc.k_norm_w),
+                                    fc.eps, fc.cos_sin.numpy(), fc.slots.numpy(), case.k_scale, case.v_scale,
+                                    okc, ovc)
+    assert np.array_equal(gen.bf16_bits(q_out), oq)
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    groups = cfg5_subset(layer, lens)
+    ref = attention_np.paged_attention_groups(oq.reshape(len(lens), 12, 72, 128), okc, ovc,
+                                              lay.block_table.numpy(), lay.seq_lens.numpy(), case.k_scale,
+                                              case.v_scale, case.sm_scale, groups, window_left=case.window_left)
+    o = out.float().cpu().numpy()
+    for (b, hk), r in ref.items():
+        assert_close(o[b, :, hk * 9:(hk + 1) * 9, :], r, f"layer {layer} sequence {b} (L={lens[b]}) KV head {hk}")
+    assert len(ref) == 8 * 8 + 56

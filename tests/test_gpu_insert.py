@@ -143,3 +143,31 @@ def test_fused_bad_position_flagged():
     f.fp8kv_device_status(clear=True)
     _fused_gpu(case, layout, 0.01, 0.01)
     assert f.fp8kv_device_status(clear=True) & f.DEV_BAD_POSITION
+
+
+def test_fused_kernel_reproduces_the_exact_arithmetic_row():
+    """The rounding-sensitive row of tests/golden/norm_rope_rounding.txt as a Q
+    head and as a K head of one token at its position: the fused kernel's q_out
+    bits equal the exact-arithmetic evaluation, and its K bytes equal the
+    E4M3 encoding of that row."""
+    from tests.test_oracle import load_norm_rope_rounding
+    fx = load_norm_rope_rounding()
+    f = fp8kv()
+    pos = fx["pos"]
+    table = torch.from_numpy(oracle.rope_table(1e6, pos + 1, 128)).cuda()
+    bf = lambda a: torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)   # noqa: E731
+    x = bf(fx["x"])
+    q = x.view(1, 1, 128).repeat(1, 2, 1).cuda()
+    k = x.view(1, 1, 128).cuda()
+    v = torch.zeros_like(k)
+    w = bf(fx["w"]).cuda()
+    q_out = torch.empty_like(q)
+    kc = torch.full((2, 1, 32, 128), POISON_E4M3, dtype=torch.uint8, device="cuda")
+    vc = kc.clone()
+    one = torch.ones(1, device="cuda")
+    f.fp8kv_qk_norm_rope_insert(q, k, v, torch.tensor([pos], device="cuda"), w, w, float(fx["eps"]), table, q_out,
+                                torch.tensor([37], device="cuda"), one, one, kc, vc)
+    got = q_out.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got[0, 0], fx["out"]) and np.array_equal(got[0, 1], fx["out"])
+    want_k = oracle.e4m3_encode(((fx["out"].astype(np.uint32) << 16).view(np.float32)))
+    assert np.array_equal(kc[1, 0, 5].cpu().numpy(), want_k)

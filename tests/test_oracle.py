@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import attention_np
 from verify_attention_gb300 import inputs as gen
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -282,14 +283,24 @@ def _small_cache(seed, seq_lens, M, ps=4, Hq=4, Hkv=2, D=128, window=None, k_sca
     return case, kc, vc
 
 
-def _run(case, kc, vc, k_scale=0.02, v_scale=0.03, window_left=None, **kw):
+# Both oracle implementations of the attention definition (the C loops and the
+# numpy float64 one used at full workload sizes) answer to the same pins.
+ATTN_IMPLS = {"c": oracle.paged_attention, "numpy": attention_np.paged_attention}
+
+
+@pytest.fixture(params=sorted(ATTN_IMPLS))
+def attn(request):
+    return ATTN_IMPLS[request.param]
+
+
+def _run(attn, case, kc, vc, k_scale=0.02, v_scale=0.03, window_left=None, **kw):
     wl = case.window_left if window_left is None else window_left
-    return oracle.paged_attention(gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(),
+    return attn(gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(),
                                   case.layout.seq_lens.numpy(), k_scale, v_scale, case.sm_scale,
                                   window_left=wl, **kw)
 
 
-def test_attention_worked_two_keys():
+def test_attention_worked_two_keys(attn):
     # q = e_0, key 0 = e_0 (code 1.0), key 1 = 0; V0 = 2.0 everywhere, V1 = 0.
     # sm_scale 1, scales 1: logits (1, 0) -> out = 2e/(1+e) in every dim.
     D = 128
@@ -299,12 +310,12 @@ def test_attention_worked_two_keys():
     vc = np.zeros((1, 1, 2, D), np.uint8)
     kc[0, 0, 0, 0] = 0x38
     vc[0, 0, 0, :] = 0x40
-    out = oracle.paged_attention(q, kc, vc, np.array([[0]], np.int32), np.array([2], np.int32),
+    out = attn(q, kc, vc, np.array([[0]], np.int32), np.array([2], np.int32),
                                  1.0, 1.0, 1.0)
     assert np.allclose(out, 2 * math.e / (1 + math.e), rtol=1e-15)
 
 
-def test_attention_brute_force_hand_enumerated_masks():
+def test_attention_brute_force_hand_enumerated_masks(attn):
     # L = 6, M = 3: rows at positions 3, 4, 5.
     visible = {-1: [[0, 1, 2, 3], [0, 1, 2, 3, 4], [0, 1, 2, 3, 4, 5]],
                2: [[1, 2, 3], [2, 3, 4], [3, 4, 5]],
@@ -315,7 +326,7 @@ def test_attention_brute_force_hand_enumerated_masks():
     vd = oracle.e4m3_decode(vc) * 0.03
     bt = case.layout.block_table.numpy()
     for wl, sets in visible.items():
-        out = _run(case, kc, vc, window_left=wl)
+        out = _run(attn, case, kc, vc, window_left=wl)
         for m in range(3):
             for h in range(4):
                 hk = h // 2
@@ -330,11 +341,11 @@ def test_attention_brute_force_hand_enumerated_masks():
                 assert np.allclose(out[0, m, h], ref, rtol=1e-12, atol=1e-14)
 
 
-def test_attention_constant_keys_give_mean_of_visible_values():
+def test_attention_constant_keys_give_mean_of_visible_values(attn):
     case, kc, vc = _small_cache(41, [37, 20], 5, ps=8, window=16)
     kc[:] = 0x3A                                   # every key equal
-    out_sw = _run(case, kc, vc)
-    out_g = _run(case, kc, vc, window_left=-1)
+    out_sw = _run(attn, case, kc, vc)
+    out_g = _run(attn, case, kc, vc, window_left=-1)
     vd = oracle.e4m3_decode(vc) * 0.03
     bt = case.layout.block_table.numpy()
     for b, L in enumerate([37, 20]):
@@ -347,51 +358,51 @@ def test_attention_constant_keys_give_mean_of_visible_values():
                     assert np.allclose(out[b, m, h], np.mean(vals, axis=0), rtol=1e-12, atol=1e-15)
 
 
-def test_attention_single_key_returns_its_value():
+def test_attention_single_key_returns_its_value(attn):
     case, kc, vc = _small_cache(51, [1], 1, ps=4)
-    out = _run(case, kc, vc)
+    out = _run(attn, case, kc, vc)
     vd = oracle.e4m3_decode(vc) * 0.03
     page = case.layout.block_table[0, 0].item()
     for h in range(4):
         assert np.allclose(out[0, 0, h], vd[page, h // 2, 0], rtol=1e-15)
 
 
-def test_attention_gqa_head_mapping():
+def test_attention_gqa_head_mapping(attn):
     case, kc, vc = _small_cache(61, [9], 2, ps=4, Hq=6, Hkv=3)
     for hk in range(3):
         vc[:, hk] = oracle.e4m3_encode(np.array([hk + 1.0], np.float32))[0]
-    out = _run(case, kc, vc, v_scale=1.0)
+    out = _run(attn, case, kc, vc, v_scale=1.0)
     for h in range(6):
         assert np.allclose(out[:, :, h], h // 2 + 1.0, rtol=1e-14)
 
 
-def test_attention_page_permutation_invariance():
+def test_attention_page_permutation_invariance(attn):
     case, kc, vc = _small_cache(71, [30, 13], 3, ps=4, window=9)
-    ref = _run(case, kc, vc)
+    ref = _run(attn, case, kc, vc)
     rng = np.random.default_rng(0)
     perm = rng.permutation(kc.shape[0])             # new page i holds old page perm[i]
     inv = np.argsort(perm)
     bt = case.layout.block_table.numpy()
     bt2 = np.where(bt >= 0, inv[np.maximum(bt, 0)], -1).astype(np.int32)
-    out = oracle.paged_attention(gen.bf16_bits(case.q), np.ascontiguousarray(kc[perm]),
+    out = attn(gen.bf16_bits(case.q), np.ascontiguousarray(kc[perm]),
                                  np.ascontiguousarray(vc[perm]), bt2, case.layout.seq_lens.numpy(),
                                  0.02, 0.03, case.sm_scale, window_left=case.window_left)
     assert np.array_equal(out, ref)
 
 
-def test_attention_equal_queries_in_group_give_equal_outputs():
+def test_attention_equal_queries_in_group_give_equal_outputs(attn):
     case, kc, vc = _small_cache(81, [25], 4, ps=8, Hq=6, Hkv=2)
     case.q[:, :, 1] = case.q[:, :, 0]
-    out = _run(case, kc, vc)
+    out = _run(attn, case, kc, vc)
     assert np.array_equal(out[:, :, 1], out[:, :, 0])
     assert not np.allclose(out[:, :, 3], out[:, :, 0])
 
 
-def test_attention_short_sequence_sliding_equals_global():
+def test_attention_short_sequence_sliding_equals_global(attn):
     case, kc, vc = _small_cache(91, [20, 7], 3, ps=4, window=20)
-    assert np.array_equal(_run(case, kc, vc), _run(case, kc, vc, window_left=-1))
+    assert np.array_equal(_run(attn, case, kc, vc), _run(attn, case, kc, vc, window_left=-1))
     case2, kc2, vc2 = _small_cache(91, [30], 3, ps=4, window=20)
-    assert not np.allclose(_run(case2, kc2, vc2), _run(case2, kc2, vc2, window_left=-1))
+    assert not np.allclose(_run(attn, case2, kc2, vc2), _run(attn, case2, kc2, vc2, window_left=-1))
 
 
 def test_attention_split_combine_equals_unsplit():
@@ -403,13 +414,13 @@ def test_attention_split_combine_equals_unsplit():
     for S in (1, 5, 8, 16, 100):
         out = oracle.paged_attention_rows(*args, rows, window_left=case.window_left, split_tokens=S)
         assert np.allclose(out, ref, rtol=1e-12, atol=1e-14)
-    full = _run(case, kc, vc)
+    full = _run(oracle.paged_attention, case, kc, vc)
     assert np.array_equal(ref.reshape(2, 4, 4, 128), full)
 
 
-def test_attention_against_torch_sdpa_float64():
+def test_attention_against_torch_sdpa_float64(attn):
     case, kc, vc = _small_cache(111, [33, 18], 5, ps=8, Hq=6, Hkv=2, window=12)
-    out = _run(case, kc, vc)
+    out = _run(attn, case, kc, vc)
     kd = oracle.e4m3_decode(kc) * 0.02
     vd = oracle.e4m3_decode(vc) * 0.03
     bt = case.layout.block_table.numpy()
@@ -427,12 +438,12 @@ def test_attention_against_torch_sdpa_float64():
         assert np.allclose(out[b], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
 
 
-def test_attention_prefill_from_empty_is_causal_sdpa():
+def test_attention_prefill_from_empty_is_causal_sdpa(attn):
     """A whole sequence as new rows (L = M = 40, a prefill from an empty cache):
     row m sees keys 0..m, which is the textbook causal attention
     (scaled_dot_product_attention with is_causal=True, no hand-built mask)."""
     case, kc, vc = _small_cache(115, [40], 40, ps=8, Hq=6, Hkv=2)
-    out = _run(case, kc, vc)
+    out = _run(attn, case, kc, vc)
     kd = oracle.e4m3_decode(kc) * 0.02
     vd = oracle.e4m3_decode(vc) * 0.03
     bt = case.layout.block_table.numpy()
@@ -443,7 +454,7 @@ def test_attention_prefill_from_empty_is_causal_sdpa():
     assert np.allclose(out[0], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
 
 
-def test_attention_prefill_chunk_constant_keys_running_mean():
+def test_attention_prefill_chunk_constant_keys_running_mean(attn):
     """A chunk of M = 24 new rows at the end of L = 50 with every key equal:
     row m (position 26 + m) returns the mean of the values it sees -- all
     earlier positions (global) or the last W = 7 (window_left 6)."""
@@ -452,7 +463,7 @@ def test_attention_prefill_chunk_constant_keys_running_mean():
     vd = oracle.e4m3_decode(vc) * 0.03
     bt = case.layout.block_table.numpy()
     for wl in (6, -1):
-        out = _run(case, kc, vc, window_left=wl)
+        out = _run(attn, case, kc, vc, window_left=wl)
         for m in range(24):
             p = 26 + m
             lo = 0 if wl < 0 else max(0, p - wl)
@@ -461,7 +472,7 @@ def test_attention_prefill_chunk_constant_keys_running_mean():
                 assert np.allclose(out[0, m, h], np.mean(vals, axis=0), rtol=1e-12, atol=1e-15)
 
 
-def test_attention_bf16_cache_variant():
+def test_attention_bf16_cache_variant(attn):
     case = gen.layer_case(121, [19], 2, 4, Hq=4, Hkv=2)
     P = case.layout.num_pages
     kc = np.zeros((P, 2, 4, 128), np.uint16)
@@ -469,7 +480,7 @@ def test_attention_bf16_cache_variant():
     for kk, vv, ss in ((case.k_prior, case.v_prior, case.slots_prior), (case.k_new, case.v_new, case.slots_new)):
         oracle.cache_insert(gen.bf16_bits(kk), gen.bf16_bits(vv), ss.numpy(), 1.0, 1.0, kc, vc,
                             cache_dtype=oracle.BF16)
-    out = oracle.paged_attention(gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(),
+    out = attn(gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(),
                                  case.layout.seq_lens.numpy(), 5.0, 7.0, case.sm_scale,
                                  cache_dtype=oracle.BF16)   # scales ignored for bf16
     kf = torch.cat([case.k_prior, case.k_new]).double()
@@ -482,15 +493,58 @@ def test_attention_bf16_cache_variant():
     assert np.allclose(out[0], ref.transpose(0, 1).numpy(), rtol=1e-10, atol=1e-12)
 
 
-def test_unvisited_pages_are_never_read():
+def test_unvisited_pages_are_never_read(attn):
     case, kc, vc = _small_cache(131, [40], 3, ps=4, window=8)
-    ref = _run(case, kc, vc)
+    ref = _run(attn, case, kc, vc)
     bt = case.layout.block_table.clone()
     bt[0, :7] = -1                                   # keys 0..27 are outside every window
-    out = oracle.paged_attention(gen.bf16_bits(case.q), kc, vc, bt.numpy(), case.layout.seq_lens.numpy(),
+    out = attn(gen.bf16_bits(case.q), kc, vc, bt.numpy(), case.layout.seq_lens.numpy(),
                                  0.02, 0.03, case.sm_scale, window_left=7)
     assert np.array_equal(out, ref)
     bt[0, 9] = -1                                    # keys 36..39 are visible: must be rejected
     with pytest.raises(ValueError):
-        oracle.paged_attention(gen.bf16_bits(case.q), kc, vc, bt.numpy(), case.layout.seq_lens.numpy(),
+        attn(gen.bf16_bits(case.q), kc, vc, bt.numpy(), case.layout.seq_lens.numpy(),
                                0.02, 0.03, case.sm_scale, window_left=7)
+
+
+@pytest.mark.parametrize("seq_lens,M,ps,window", [([300, 77], 12, 32, 100), ([130], 40, 64, None)])
+def test_numpy_and_c_attention_agree(seq_lens, M, ps, window):
+    """The two oracle implementations of one definition agree to float64
+    rounding on a verifier-shaped layer (72/8 heads) and a prefill chunk."""
+    case = gen.layer_case(141 + M, seq_lens, M, ps, window=window)
+    P = case.layout.num_pages
+    kc = np.full((P, 8, ps, 128), 0xA5, np.uint8)
+    vc = kc.copy()
+    for kk, vv, ss in ((case.k_prior, case.v_prior, case.slots_prior), (case.k_new, case.v_new, case.slots_new)):
+        oracle.cache_insert(gen.bf16_bits(kk), gen.bf16_bits(vv), ss.numpy(), case.k_scale, case.v_scale, kc, vc)
+    args = (gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(), case.layout.seq_lens.numpy(),
+            case.k_scale, case.v_scale, case.sm_scale)
+    a = oracle.paged_attention(*args, window_left=case.window_left)
+    b = attention_np.paged_attention(*args, window_left=case.window_left)
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+
+
+def load_norm_rope_rounding():
+    """The exact-arithmetic row of tests/golden/norm_rope_rounding.txt."""
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "norm_rope_rounding.txt")):
+        if line.strip() and not line.startswith("#"):
+            key, *rest = line.split()
+            vals[key] = rest
+    hexes = lambda k, t: np.array([int(h, 16) for h in vals[k]], t)   # noqa: E731
+    return dict(x=hexes("x", np.uint16), w=hexes("w", np.uint16), cs=hexes("cs", np.uint32).view(np.float32),
+                out=hexes("out", np.uint16), eps=np.uint32(int(vals["eps"][0], 16)).view(np.float32),
+                pos=int(vals["pos"][0]))
+
+
+def test_norm_rope_rounding_sensitive_fixture():
+    """A row whose output bits change if the bf16 rounding after the
+    normalisation is dropped, if the 32 lane sums are added sequentially
+    instead of pairwise, or if RoPE rounds its product before the fma: the
+    oracle must reproduce the exact-arithmetic evaluation bit for bit."""
+    f = load_norm_rope_rounding()
+    assert f["eps"] == np.float32(1e-6)
+    table = oracle.rope_table(1e6, f["pos"] + 1, 128)
+    assert np.array_equal(table[f["pos"]], f["cs"])             # the stored row is the model's table row
+    out = oracle.norm_rope_row(f["x"], f["w"], float(f["eps"]), f["cs"])
+    assert np.array_equal(out, f["out"]), np.nonzero(out != f["out"])
