@@ -641,6 +641,44 @@ static bool make_cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, 
     return r == CUDA_SUCCESS;
 }
 
+// Tensor maps by (cache base, dtype, heads, page size, pages): a map is a pure
+// function of these, so repeated calls over the same persistent cache reuse
+// it instead of encoding it again.  A small direct-mapped table per process.
+struct MapKey {
+    const void* base;
+    int fp8, Hkv, PS, num_pages;
+    bool operator==(const MapKey& o) const {
+        return base == o.base && fp8 == o.fp8 && Hkv == o.Hkv && PS == o.PS && num_pages == o.num_pages;
+    }
+};
+
+static bool cached_cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int num_pages) {
+    constexpr int kSlots = 512;
+    struct Entry {
+        MapKey key;
+        CUtensorMap map;
+        bool valid;
+    };
+    static Entry table[kSlots];
+    static std::mutex mu;
+    const MapKey key{base, fp8 ? 1 : 0, Hkv, PS, num_pages};
+    const size_t h = ((reinterpret_cast<uintptr_t>(base) >> 8) ^ (size_t)num_pages * 131 ^ (size_t)PS * 7 ^
+                      (size_t)Hkv * 3 ^ (size_t)key.fp8) % kSlots;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (table[h].valid && table[h].key == key) {
+            *m = table[h].map;
+            return true;
+        }
+    }
+    if (!make_cache_map(m, base, fp8, Hkv, PS, num_pages)) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    table[h].key = key;
+    table[h].map = *m;
+    table[h].valid = true;
+    return true;
+}
+
 struct Plan {
     int split_pages, num_splits, split_tokens;
 };
@@ -817,8 +855,8 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     if (need && (!workspace || workspace_bytes < need || !al16(workspace))) return FP8KV_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    if (!make_cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||
-        !make_cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
+    if (!cached_cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||
+        !cached_cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
         return FP8KV_ERR_CUDA;
 
     AttnParams P = {};

@@ -72,14 +72,15 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def _ptr(t: Optional[torch.Tensor]):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    # plain ints: ctypes converts them for c_void_p arguments without a wrapper object
+    return t.data_ptr() if t is not None else 0
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 def _check(fn, rc):
