@@ -408,6 +408,11 @@ def capture_step_graphs(w: Workload, stream):
     return graphs, launches
 
 
+def layers_of_kind(w: Workload, window_left):
+    """Every layer (all cache copies) of one kind (-1 = global)."""
+    return [c[li] for c in w.copies for li, l in enumerate(w.copies[0]) if l.window_left == window_left]
+
+
 def dominant_kernel(w: Workload, stream, reps=24):
     """Average device duration of the attention call (partial kernel + reduce) on
     the layer kind with the most bytes.  `reps` calls, rotating over cache copies
@@ -418,14 +423,32 @@ def dominant_kernel(w: Workload, stream, reps=24):
     top = max(b for b, _ in cands)
     idx = [li for b, li in cands if b == top]
     layers = [c[li] for c in w.copies for li in idx]
+    secs, dispatch = time_attention_calls(layers, stream, w.ws, reps)
+    return top, secs, flops_of(layers[0]), dispatch
+
+
+def flops_of(layer):
+    return layer.flops()
+
+
+def time_attention_calls(layers, stream, ws, reps=24, step=False):
+    """Median device time of one attention call (partial kernel + reduce, as
+    one fp8kv_paged_attention call; with step=True the layer's whole step, new
+    tokens into the cache then attention), `reps` calls rotating over `layers`
+    (other cache copies, so the reads come from HBM) captured in one CUDA
+    graph; also the dispatch marker of the last call."""
+    from verify_attention_gb300 import fp8kv
+
+    def call(layer):
+        (layer.step if step else layer.attend)(ws)
     with torch.cuda.stream(stream):
         for i in range(3):
-            layers[i % len(layers)].attend(w.ws)
+            call(layers[i % len(layers)])
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for i in range(reps):
-            layers[i % len(layers)].attend(w.ws)
+            call(layers[i % len(layers)])
     with torch.cuda.stream(stream):
         g.replay()
     torch.cuda.synchronize()
@@ -439,12 +462,28 @@ def dominant_kernel(w: Workload, stream, reps=24):
         b.synchronize()
         per_call.append(a.elapsed_time(b) / reps)
     del g
-    from verify_attention_gb300 import fp8kv
-    return top, statistics.median(per_call) / 1e3, flops_of(layers[0]), fp8kv.fp8kv_last_dispatch()
+    return statistics.median(per_call) / 1e3, fp8kv.fp8kv_last_dispatch()
 
 
-def flops_of(layer):
-    return layer.flops()
+def rotating_copies(layer, n):
+    """n views of one layer that share its queries and metadata but each own a
+    copy of its caches (and an output buffer), so that consecutive calls over
+    them read from HBM even when one layer fits in L2."""
+    import copy
+    out = []
+    for _ in range(n):
+        c = copy.copy(layer)
+        c.kc = layer.kc.clone()
+        c.vc = layer.vc.clone()
+        c.out = torch.empty_like(layer.out)
+        out.append(c)
+    return out
+
+
+def call_record(layer, secs, dispatch, hbm_peak):
+    b = layer.attn_bytes()
+    return {"us": secs * 1e6, "algorithmic_bytes": b, "gbs": b / secs / 1e9, "frac_of_hbm": b / secs / 1e9 / hbm_peak,
+            "dispatch": dispatch}
 
 
 def _packed(tensors, device, align=256, pin=False):
@@ -639,6 +678,90 @@ def cpu_baseline(name, page_size, target_s=12.0):
             "sample": s.describe(n) + f"; host has {os.cpu_count()} cores"}
 
 
+# ------------------------------------------------------ side measurements
+
+def _step_time(w, stream, steps=10, warmup=3):
+    graphs, launches = capture_step_graphs(w, stream)
+    secs = time_graphs(graphs, steps, warmup, stream) / steps
+    del graphs
+    return secs, launches
+
+
+def side_measurements(dev, stream, hbm_peak, bf16_peak):
+    """The A/B runs and the other configurations, each under its own key of
+    the one JSON line (device time, CUDA-graph replays, caches rotated or
+    larger than L2):
+      verify48_page64  the 48-layer step at page 64 (the page-size A/B);
+      decode128k       12 long-context decode layers, E4M3 and BF16 cache;
+      prefill16k       a prefill chunk on the tensor cores;
+      serving64        the batched serving mix, per layer kind;
+      cfg1, cfg2       the single-layer configurations (rotating cache copies)."""
+    out = {}
+    torch.cuda.empty_cache()
+    w = build_workload("verify48", 64, dev)
+    s64, n64 = _step_time(w, stream, steps=20)
+    b64 = w.bytes_per_step()
+    calls = {}
+    for kind, wl in (("sliding_512", 511), ("global", -1)):
+        ls = layers_of_kind(w, wl)
+        secs, disp = time_attention_calls(ls, stream, w.ws)
+        calls[kind] = call_record(ls[0], secs, disp, hbm_peak)
+    out["verify48_page64"] = {"ms_per_step": s64 * 1e3, "verify_steps_per_s": 1 / s64, "gbs": b64 / s64 / 1e9,
+                              "frac_of_hbm": b64 / s64 / 1e9 / hbm_peak, "algorithmic_bytes_per_step": b64,
+                              "launches_per_step": n64, "attention_calls": calls}
+    del w
+    torch.cuda.empty_cache()
+    dec = {}
+    for dt in ("e4m3", "bf16"):
+        w = build_workload("decode128k", 64, dev, cache_dtype=dt)
+        s2, _ = _step_time(w, stream, steps=5)
+        b2, t2, _, d2 = dominant_kernel(w, stream, reps=12)
+        dec[dt] = {"gbs_step": w.bytes_per_step() / s2 / 1e9, "ms_per_step": s2 * 1e3,
+                   "attention_gbs": b2 / t2 / 1e9, "attention_frac": b2 / t2 / 1e9 / hbm_peak,
+                   "attention_ms": t2 * 1e3, "attention_bytes": b2, "dispatch": d2}
+        del w
+        torch.cuda.empty_cache()
+    out["decode128k"] = {**dec["e4m3"], "bf16": dec["bf16"],
+                         "fp8_over_bf16_step_speedup": dec["bf16"]["ms_per_step"] / dec["e4m3"]["ms_per_step"],
+                         "fp8_over_bf16_attention_speedup": dec["bf16"]["attention_ms"] / dec["e4m3"]["attention_ms"]}
+    w = build_workload("prefill16k", 64, dev)
+    s3, _ = _step_time(w, stream, steps=5)
+    _, t3, f3, d3 = dominant_kernel(w, stream, reps=8)
+    out["prefill16k"] = {"ms_per_step": s3 * 1e3, "tflops_step": w.flops_per_step() / s3 / 1e12,
+                         "attention_ms": t3 * 1e3, "attention_tflops": f3 / t3 / 1e12,
+                         "attention_frac_of_bf16_peak": f3 / t3 / 1e12 / bf16_peak, "dispatch": d3}
+    del w
+    torch.cuda.empty_cache()
+    w = build_workload("serving64", 32, dev)
+    s5, n5 = _step_time(w, stream, steps=5)
+    srv = {"ms_per_step": s5 * 1e3, "gbs_step": w.bytes_per_step() / s5 / 1e9,
+           "frac_of_hbm_step": w.bytes_per_step() / s5 / 1e9 / hbm_peak, "launches_per_step": n5}
+    for kind, wl in (("global", -1), ("sliding_512", 511)):
+        ls = layers_of_kind(w, wl)
+        secs, disp = time_attention_calls(ls, stream, w.ws, reps=8)
+        srv[kind] = call_record(ls[0], secs, disp, hbm_peak)
+    out["serving64"] = srv
+    del w
+    torch.cuda.empty_cache()
+    small = {}
+    for name, case, copies in (("cfg1_tiny_decode", gen.cfg1_case(device=dev), 256),
+                               ("cfg2_verify_global", gen.cfg2_case(None, device=dev), 40),
+                               ("cfg2_verify_sliding_512", gen.cfg2_case(512, device=dev), 40)):
+        base = Layer(case, dev)
+        ws = torch.empty(max(base.ws_bytes, 16), dtype=torch.uint8, device=dev)
+        ls = rotating_copies(base, copies)
+        secs, disp = time_attention_calls(ls, stream, ws, reps=48)
+        rec = call_record(base, secs, disp, hbm_peak)
+        ssecs, _ = time_attention_calls(ls, stream, ws, reps=48, step=True)
+        rec["step_us"] = ssecs * 1e6
+        rec["step"] = "append of the new tokens + attention (one fp8kv_append_paged_attention call)"
+        small[name] = rec
+        del ls, base, ws
+    out.update(small)
+    torch.cuda.empty_cache()
+    return out
+
+
 # -------------------------------------------------------------------- main
 
 def dist_setup():
@@ -720,7 +843,8 @@ def main():
     ap.add_argument("--page-size", type=int, default=32, choices=[32, 64])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extra", action="store_true", help="skip the decode128k side measurement")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the side measurements (page-64 step, decode, prefill, serving mix, single layers)")
     ap.add_argument("--layers", type=int, default=None, help="fewer layers (small profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -812,26 +936,16 @@ def main():
                                  "traffic_source": "no capture for this kernel and workload",
                                  "gbs": achieved,
                                  "peak_source": f"{peak_src} bf16_tflops (MEASURED_PEAKS.json)"})
+    if args.workload == "verify48":
+        # the step's two attention-call kinds, each against HBM
+        line["attention_calls"] = {}
+        for kind, wl in (("sliding_512", 511), ("global", -1)):
+            ls = layers_of_kind(w, wl)
+            secs, disp = time_attention_calls(ls, stream, w.ws)
+            line["attention_calls"][kind] = call_record(ls[0], secs, disp, hbm_peak)
     if rank == 0 and args.workload == "verify48" and not args.no_extra:
-        # the long-context decode gate: its own step and dominant kernel
         del graphs
-        w2 = build_workload("decode128k", 64, dev)
-        g2, _ = capture_step_graphs(w2, stream)
-        s2 = time_graphs(g2, 5, 3, stream) / 5
-        b2, t2, _, d2 = dominant_kernel(w2, stream, reps=12)
-        line["decode128k"] = {"gbs_step": w2.bytes_per_step() / s2 / 1e9, "ms_per_step": s2 * 1e3,
-                              "attention_gbs": b2 / t2 / 1e9, "attention_frac": b2 / t2 / 1e9 / hbm_peak,
-                              "attention_ms": t2 * 1e3, "dispatch": d2}
-        del g2, w2
-        # a prefill chunk on the same kernel (row tiles): bound by the tensor cores
-        w3 = build_workload("prefill16k", 64, dev)
-        g3, _ = capture_step_graphs(w3, stream)
-        s3 = time_graphs(g3, 5, 3, stream) / 5
-        _, t3, f3, d3 = dominant_kernel(w3, stream, reps=8)
-        line["prefill16k"] = {"ms_per_step": s3 * 1e3, "tflops_step": w3.flops_per_step() / s3 / 1e12,
-                              "attention_ms": t3 * 1e3, "attention_tflops": f3 / t3 / 1e12,
-                              "attention_frac_of_bf16_peak": f3 / t3 / 1e12 / bf16_peak, "dispatch": d3}
-        del g3, w3
+        line.update(side_measurements(dev, stream, hbm_peak, bf16_peak))
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, ps)
     if rank == 0:

@@ -133,43 +133,46 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         bool ok = true;
         int issued = 0;
-        // page ids 32 at a time, the next batch loaded while this one is issued
-        int next = (lane < n_pages) ? bt[lane] : 0;
-        for (int base = 0; base < n_pages && ok; base += 32) {
-            const int mine = next;
-            if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
-            const int cnt = min(32, n_pages - base);
-            for (int j = 0; j < cnt; ++j) {
-                const int phys = __shfl_sync(0xffffffffu, mine, j);
-                const int i = base + j;
-                const int jj = i / P.KW, use = jj / SG;
-                const int s = (i % P.KW) * SG + jj % SG;
-                if (lane == 0) {
-                    if (use > 0) ok = mbar_wait(smem_u32(&bars[S + s]), (use - 1) & 1);
-                    if (ok) {
-                        const uint32_t full = smem_u32(&bars[s]);
-                        const uint32_t dk = smem_u32(smem + s * C::kStageBytes);
-                        const uint32_t dv = dk + C::kTileBytes;
-                        mbar_expect_tx(full, C::kStageBytes);
-                        if (FP8) {
-                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
-                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
-                        } else {
-                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
-                            tma_load_3d(dk + PS * 128, &tm_k, 64, hk * PS, phys, full, policy);
-                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
-                            tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
-                        }
+        // One batch = one page per stage (NS <= 32 pages, lane j owns stage
+        // s(j)); the lanes wait for their own stages and issue their copies
+        // together -- one lane issuing every copy in turn caps the staging
+        // rate well below HBM's.  The next batch's page ids are loaded while
+        // this one is issued.
+        const int NS = P.KW * SG;
+        const int jj_l = lane / P.KW;
+        const int s_l = (lane % P.KW) * SG + jj_l % SG;   // stage of lane's page in every batch
+        int next = (lane < NS && lane < n_pages) ? bt[lane] : 0;
+        for (int base = 0; base < n_pages; base += NS) {
+            const int phys = next;
+            if (base + NS < n_pages) next = (lane < NS && base + NS + lane < n_pages) ? bt[base + NS + lane] : 0;
+            const int use = base / NS;
+            const bool mine = lane < NS && base + lane < n_pages;
+            bool okl = true;
+            if (mine) {
+                if (use > 0) okl = mbar_wait(smem_u32(&bars[S + s_l]), (use - 1) & 1);
+                if (okl) {
+                    const uint32_t full = smem_u32(&bars[s_l]);
+                    const uint32_t dk = smem_u32(smem + s_l * C::kStageBytes);
+                    const uint32_t dv = dk + C::kTileBytes;
+                    mbar_expect_tx(full, C::kStageBytes);
+                    if (FP8) {
+                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                        tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                    } else {
+                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                        tma_load_3d(dk + PS * 128, &tm_k, 64, hk * PS, phys, full, policy);
+                        tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                        tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                ++issued;
             }
+            ok = __all_sync(0xffffffffu, okl);
+            if (!ok) break;
+            issued = min(n_pages, base + NS);
         }
         // Do not leave while copies into this CTA's shared memory are in flight.
         if (lane == 0) {
-            for (int i = max(0, issued - P.KW * SG); i < issued; ++i) {
+            for (int i = max(0, issued - NS); i < issued; ++i) {
                 const int jj = i / P.KW;
                 mbar_wait(smem_u32(&bars[(i % P.KW) * SG + jj % SG]), (jj / SG) & 1);
             }
@@ -546,45 +549,67 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     const int first_page = lo0 / page_size, last_page = (L - M + (R0 + RL - 1) / G) / page_size;
     const int ns = (last_page - first_page + split_pages) / split_pages;
     if (ns <= 1 || ns > num_splits) return;
-    // partition weights: lane j owns partitions j, j+32, ...
     const float* ml = ws_ml + row * num_splits * 2;
-    float mstar = -INFINITY;
-    for (int s = lane; s < ns; s += 32) mstar = fmaxf(mstar, ml[2 * s]);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-    float den = 0.f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* po = ws_o + row * num_splits * 128 + lane * 4;
-    for (int base = 0; base < ns; base += 32) {
-        const int s_l = base + lane;
-        float w_l = 0.f;
-        if (s_l < ns) {
-            const float ms = ml[2 * s_l];
-            w_l = (ms == -INFINITY) ? 0.f : ex2(ms - mstar);
-            den += w_l * ml[2 * s_l + 1];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+    if (ns <= 16) {
+        // every load in flight at once: lane j's (max, sum) of partition j and
+        // this lane's four dims of every partition; then the arithmetic
+        const float2 mlj = lane < ns ? *(const float2*)(ml + 2 * lane) : make_float2(-INFINITY, 0.f);
+        float4 v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = u < ns ? *(const float4*)(po + (int64_t)u * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float mstar = mlj.x;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+        const float w_l = (mlj.x == -INFINITY) ? 0.f : ex2(mlj.x - mstar);
+        den = w_l * mlj.y;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const float w = __shfl_sync(0xffffffffu, w_l, u);       // 0 past ns
+            acc.x += w * v[u].x;
+            acc.y += w * v[u].y;
+            acc.z += w * v[u].z;
+            acc.w += w * v[u].w;
         }
-        const int cnt = min(32, ns - base);
-        int j = 0;
-        for (; j + 4 <= cnt; j += 4) {         // four partial rows in flight
-            float4 v[4];
+    } else {
+        // partition weights: lane j owns partitions j, j+32, ...
+        float mstar = -INFINITY;
+        for (int s = lane; s < ns; s += 32) mstar = fmaxf(mstar, ml[2 * s]);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) v[u] = *(const float4*)(po + (int64_t)(base + j + u) * 128);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float w = __shfl_sync(0xffffffffu, w_l, j + u);
-                acc.x += w * v[u].x;
-                acc.y += w * v[u].y;
-                acc.z += w * v[u].z;
-                acc.w += w * v[u].w;
+        for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+        for (int base = 0; base < ns; base += 32) {
+            const int s_l = base + lane;
+            float w_l = 0.f;
+            if (s_l < ns) {
+                const float ms = ml[2 * s_l];
+                w_l = (ms == -INFINITY) ? 0.f : ex2(ms - mstar);
+                den += w_l * ml[2 * s_l + 1];
             }
-        }
-        for (; j < cnt; ++j) {
-            const float w = __shfl_sync(0xffffffffu, w_l, j);
-            const float4 v = *(const float4*)(po + (int64_t)(base + j) * 128);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+            const int cnt = min(32, ns - base);
+            int j = 0;
+            for (; j + 8 <= cnt; j += 8) {         // eight partial rows in flight
+                float4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = *(const float4*)(po + (int64_t)(base + j + u) * 128);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float w = __shfl_sync(0xffffffffu, w_l, j + u);
+                    acc.x += w * v[u].x;
+                    acc.y += w * v[u].y;
+                    acc.z += w * v[u].z;
+                    acc.w += w * v[u].w;
+                }
+            }
+            for (; j < cnt; ++j) {
+                const float w = __shfl_sync(0xffffffffu, w_l, j);
+                const float4 v = *(const float4*)(po + (int64_t)(base + j) * 128);
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
         }
     }
 #pragma unroll
@@ -896,6 +921,7 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
         while (kw * sg * stage_bytes < merge) ++sg;
         P.KW = kw;
         P.SG = sg;
+        if (kw * sg > 32) return FP8KV_ERR_UNSUPPORTED;   // the producer gives each lane one stage
     }
     P.window_left = window_left;
     P.split_pages = plan.split_pages;

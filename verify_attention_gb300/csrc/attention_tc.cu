@@ -74,8 +74,8 @@ enum {
     B_Q_READY = B_O_FINAL + 1,
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                    // one per TMEM lane quarter: the two softmax warps
-    B_NEW = B_PAIR + 4,                         // append: the new tokens are in the cache
-    B_COUNT = B_NEW + 1
+    B_PATCH = B_PAIR + 4,                       // append: new tokens patched into the staged tile
+    B_COUNT = B_PATCH + 1
 };
 
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         mbar_init(bar(B_O_FINAL), 1);
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
-        mbar_init(bar(B_NEW), CONV_WARPS);
+        mbar_init(bar(B_PATCH), CONV_WARPS);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
@@ -174,6 +174,25 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
+        }
+    }
+    if (warp == 1 && lane == 0) {
+        // L2 prefetch of the block-table entries this partition will read,
+        // located from a read of the sequence length made before the wait for
+        // the previous kernel: a hint only (the length and the entries used
+        // below are read after the wait), it takes the dependent DRAM round
+        // trip of the block table off the path to the first page copy
+        const int Lg = *(volatile const int*)(P.seq_lens + b);
+        if (Lg >= P.M && Lg <= P.max_seq_len) {
+            const int hi_g = Lg - P.M + (R0 + RL - 1) / P.G;
+            const int lo_g = (P.window_left >= 0) ? max(0, Lg - P.M + R0 / P.G - P.window_left) : 0;
+            const int pb = lo_g / PS + split * P.split_pages;
+            const int pe = min(pb + P.split_pages, hi_g / PS + 1);
+            const int32_t* row = P.block_table + (int64_t)b * P.mpps;
+            const uintptr_t a0 = reinterpret_cast<uintptr_t>(row + pb) & ~(uintptr_t)127;
+            const uintptr_t a1 = reinterpret_cast<uintptr_t>(row + min(pe, P.mpps));
+            for (uintptr_t a = a0; a < a1; a += 128)        // 128-byte lines, usually one
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
         }
     }
     fence_before();
@@ -205,6 +224,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     // append: new tokens at positions [L - M, L) that fall in this partition
     const int app_lo = max(L - P.M, k_begin), app_hi = min(L, k_begin + n_pages * PS);
     const bool appends = P.k_new != nullptr && run && app_lo < app_hi;
+    // Appended tokens are written to the cache in global memory and, so that
+    // no load has to wait for that write, also patched into the staged copy of
+    // the tile that holds them (which may have been loaded with the old bytes):
+    // tiles app_t0 .. app_t1 of this partition.
+    const int app_t0 = appends ? (app_lo - k_begin) / NK : 1 << 30;
+    const int app_t1 = appends ? (app_hi - 1 - k_begin) / NK : -1;
     bool ok = true;
 
     if (!run) {
@@ -213,45 +238,40 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // ---------------------------------------------------------- producer
         const uint64_t policy = policy_evict_first();
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
-        int issued = 0;
-        bool new_seen = false;
-        // page ids 32 at a time, the next batch loaded while this one is issued
+        int issued_tiles = 0;
+        // page ids 32 at a time (whole tiles: PPT divides 32), the next batch
+        // loaded while this one is issued; the boxes of a tile (K and V of its
+        // PPT pages) go out in one instruction, lane i issuing box i -- one
+        // lane issuing them in turn caps the staging rate well below HBM's
         int next = (lane < n_pages) ? bt[lane] : 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
             const int mine = next;
             if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
             const int cnt = min(32, n_pages - base);
-            for (int j = 0; j < cnt; ++j) {
-                const int phys = __shfl_sync(0xffffffffu, mine, j);
-                const int i = base + j;
-                const int t = i / PPT, pin = i % PPT;
-                const int s = t % STAGES, use = t / STAGES;
+            for (int j0 = 0; j0 < cnt; j0 += PPT) {
+                const int t = (base + j0) / PPT, s = t % STAGES, use = t / STAGES;
+                const int pages_here = min(PPT, n_pages - t * PPT);
                 if (lane == 0) {
-                    // a page holding appended tokens is loaded once they are written
-                    const int pk = (page_begin + i) * PS;
-                    if (appends && pk < app_hi && pk + PS > app_lo && !new_seen) {
-                        ok = mbar_wait(bar(B_NEW), 0);
-                        new_seen = true;
-                    }
-                    if (pin == 0) {
-                        if (use > 0 && ok) ok = mbar_wait(bar(B_STG_EMPTY + s), (use - 1) & 1);
-                        const int pages_here = min(PPT, n_pages - t * PPT);
-                        if (ok) mbar_expect_tx(bar(B_STG_FULL + s), pages_here * PS * 128 * 2);
-                    }
-                    if (ok) {
-                        const uint32_t dk = smem_u32(stg + s * STG_BYTES + pin * PS * 128);
-                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
-                        tma_load_3d(dk + STG_K, &tm_v, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
-                    }
+                    if (use > 0) ok = mbar_wait(bar(B_STG_EMPTY + s), (use - 1) & 1);
+                    if (ok) mbar_expect_tx(bar(B_STG_FULL + s), pages_here * PS * 128 * 2);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
-                issued = i + 1;
+                const int pin = lane % PPT;                 // lanes 0..PPT-1: K boxes, PPT..2PPT-1: V boxes
+                const int phys = __shfl_sync(0xffffffffu, mine, j0 + pin);
+                if (lane < 2 * PPT && pin < pages_here) {
+                    const uint32_t dk = smem_u32(stg + s * STG_BYTES + pin * PS * 128);
+                    if (lane < PPT)
+                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
+                    else
+                        tma_load_3d(dk + STG_K, &tm_v, 0, hk * PS, phys, bar(B_STG_FULL + s), policy);
+                }
+                __syncwarp();
+                issued_tiles = t + 1;
             }
         }
         if (lane == 0) {   // never leave with copies into this CTA's shared memory in flight
-            const int t_issued = (issued + PPT - 1) / PPT;
-            for (int t = max(0, t_issued - STAGES); t < t_issued; ++t)
+            for (int t = max(0, issued_tiles - STAGES); t < issued_tiles; ++t)
                 mbar_wait(bar(B_STG_FULL + t % STAGES), (t / STAGES) & 1);
         }
     } else if (warp == 1) {
@@ -265,6 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 if (t < n_tiles) {
                     const int s = t % STAGES, sb = t & 1;
                     ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);
+                    if (ok && t >= app_t0 && t <= app_t1) ok = mbar_wait(bar(B_PATCH), (t - app_t0) & 1);
                     if (!ok) break;
                     fence_after();
                     const uint32_t kt = smem_u32(stg + s * STG_BYTES);
@@ -306,29 +327,41 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // Keys outside every row's range are written as zeros, so stale or NaN
         // bytes there cannot reach the output.
         const int ct = converter_index(warp) * 32 + lane;
-        if (appends) {
-            // ---------------------------------------------- append insert
-            // the converter warps encode this head's appended tokens (the
-            // cache-insert encoding, one 8-element chunk of K and of V per
-            // item) into the cache, then let the producer load those pages
-            const int n = app_hi - app_lo;
-            const float ksc = *P.k_scale, vsc = *P.v_scale;
-            for (int it = ct; it < n * 16; it += CONV_THREADS) {
-                const int pos = app_lo + (it >> 4), chunk = it & 15, m = pos - (L - P.M);
-                const int64_t src = (((int64_t)b * P.M + m) * P.Hkv + hk) * 16 + chunk;
-                const uint4 kx = ((const uint4*)P.k_new)[src], vx = ((const uint4*)P.v_new)[src];
-                const int page = P.block_table[(int64_t)b * P.mpps + pos / PS];
-                if (page < 0 || page >= P.num_pages) {
-                    if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
-                    continue;
-                }
-                const int64_t dst = (((int64_t)page * P.Hkv + hk) * PS + pos % PS) * 128 + chunk * 8;
-                *(uint2*)(P.k_cache + dst) = e4m3_encode8(kx, ksc);
-                *(uint2*)(P.v_cache + dst) = e4m3_encode8(vx, vsc);
+        const int n_app = appends ? app_hi - app_lo : 0;
+        const float ksc = appends ? *P.k_scale : 1.f, vsc = appends ? *P.v_scale : 1.f;
+        // the append item `it`: one 8-element chunk of K and of V of a new token
+        auto app_item = [&](int it, uint2& kc, uint2& vc, int& pos, int& chunk) {
+            pos = app_lo + (it >> 4);
+            chunk = it & 15;
+            const int m = pos - (L - P.M);
+            const int64_t src = (((int64_t)b * P.M + m) * P.Hkv + hk) * 16 + chunk;
+            kc = e4m3_encode8(((const uint4*)P.k_new)[src], ksc);
+            vc = e4m3_encode8(((const uint4*)P.v_new)[src], vsc);
+        };
+        // ---------------------------------------------------- append insert
+        // the new tokens of this head into the cache (the cache-insert
+        // encoding); the staged tiles get the same bytes below (each thread
+        // keeps its first item's codes for that)
+        uint2 kc0 = make_uint2(0, 0), vc0 = make_uint2(0, 0);
+        int pos0 = -1, chunk0 = 0;
+        for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
+            uint2 kc, vc;
+            int pos, chunk;
+            app_item(it, kc, vc, pos, chunk);
+            if (it == ct) {
+                kc0 = kc;
+                vc0 = vc;
+                pos0 = pos;
+                chunk0 = chunk;
             }
-            asm volatile("fence.proxy.async.global;" ::: "memory");   // generic writes before the TMA reads
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_NEW));
+            const int page = P.block_table[(int64_t)b * P.mpps + pos / PS];
+            if (page < 0 || page >= P.num_pages) {
+                if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
+                continue;
+            }
+            const int64_t dst = (((int64_t)page * P.Hkv + hk) * PS + pos % PS) * 128 + chunk * 8;
+            *(uint2*)(P.k_cache + dst) = kc;
+            *(uint2*)(P.v_cache + dst) = vc;
         }
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % STAGES, vb = t % VBUFS;
@@ -336,6 +369,27 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             if (ok && t >= VBUFS) ok = mbar_wait(bar(B_V_EMPTY + vb), ((t / VBUFS) - 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const int k0 = k_begin + t * NK;
+            if (t >= app_t0 && t <= app_t1) {
+                // patch this tile's new rows (K and V, 128-byte swizzled rows of
+                // the staging buffer) with the appended tokens' codes
+                uint8_t* kst = stg + s * STG_BYTES;
+                for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
+                    uint2 kc = kc0, vc = vc0;
+                    int pos = pos0, chunk = chunk0;
+                    if (it != ct) app_item(it, kc, vc, pos, chunk);
+                    const int r = pos - k0;
+                    if (r < 0 || r >= NK) continue;
+                    const int off = r * 128 + ((((chunk >> 1) ^ r) & 7) << 4) + (chunk & 1) * 8;
+                    *(uint2*)(kst + off) = kc;
+                    *(uint2*)(kst + STG_K + off) = vc;
+                }
+                fence_proxy_async();                        // for the tensor cores' read of K
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_PATCH));
+                // every converter warp's rows are in place before V is read
+                ok = mbar_wait(bar(B_PATCH), (t - app_t0) & 1);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            }
             const int pages_here = min(PPT, n_pages - t * PPT);
             const int zlo = max(0, min(NK, lo0 - k0));
             const int zhi = max(0, min(min(NK, pages_here * PS), hi0 + 1 - k0));
@@ -626,41 +680,56 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         __syncwarp();
         cluster_sync_all();
         if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
+            const float vsc = *P.v_scale;
             const int hh = lane >> 4;                       // staged half row of these dims
-            for (int r = split + P.cluster * warp; r < RL; r += P.cluster * WARPS) {
-                // every remote load of the row first (one round trip), then the arithmetic
-                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 8;
-                uint2 v[8];
+            const int stride = P.cluster * WARPS;
+            // rows r and r + stride together: every remote load of both rows
+            // first (one round trip), then the arithmetic
+            for (int r = split + P.cluster * warp; r < RL; r += 2 * stride) {
+                const int rows[2] = {r, r + stride};
+                uint2 v[2][8];
+                float mp[2], lp[2];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) v[p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
-                float mp = -INFINITY, lp = 0.f;
-                if (lane < nsplit_b) {
-                    mp = ld_dsmem_f32(dsmem_addr(&xch[r], lane));
-                    lp = ld_dsmem_f32(dsmem_addr(&xch[128 + r], lane));
+                for (int q = 0; q < 2; ++q) {
+                    const int rq = min(rows[q], RL - 1);
+                    const uint8_t* src = stg + (hh * 128 + rq) * EPI_STRIDE + (lane & 15) * 8;
+#pragma unroll
+                    for (int p = 0; p < 8; ++p)
+                        v[q][p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
+                    mp[q] = -INFINITY;
+                    lp[q] = 0.f;
+                    if (lane < nsplit_b) {
+                        mp[q] = ld_dsmem_f32(dsmem_addr(&xch[rq], lane));
+                        lp[q] = ld_dsmem_f32(dsmem_addr(&xch[128 + rq], lane));
+                    }
                 }
-                float mstar = mp;
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-                // partition weight 2^(m_p - m*) l_p on its normalised partial
-                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar) * lp;
-                float lsum = w;
+                for (int q = 0; q < 2; ++q) {
+                    if (rows[q] >= RL) break;
+                    float mstar = mp[q];
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+                    // partition weight 2^(m_p - m*) l_p on its normalised partial
+                    const float w = (mp[q] == -INFINITY) ? 0.f : ex2(mp[q] - mstar) * lp[q];
+                    float lsum = w;
 #pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
-                    const float2 a = f16x2_to_f32x2(v[p].x), c2 = f16x2_to_f32x2(v[p].y);
-                    acc.x = fmaf(wp, a.x, acc.x);
-                    acc.y = fmaf(wp, a.y, acc.y);
-                    acc.z = fmaf(wp, c2.x, acc.z);
-                    acc.w = fmaf(wp, c2.y, acc.w);
+                    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) {
+                        const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
+                        const float2 a = f16x2_to_f32x2(v[q][p].x), c2 = f16x2_to_f32x2(v[q][p].y);
+                        acc.x = fmaf(wp, a.x, acc.x);
+                        acc.y = fmaf(wp, a.y, acc.y);
+                        acc.z = fmaf(wp, c2.x, acc.z);
+                        acc.w = fmaf(wp, c2.y, acc.w);
+                    }
+                    const float inv = vsc / lsum;
+                    const int m = (R0 + rows[q]) / P.G;
+                    const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + rows[q]) % P.G;
+                    *(uint2*)(P.out + orow * 128 + 4 * lane) =
+                        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
                 }
-                const float inv = *P.v_scale / lsum;
-                const int m = (R0 + r) / P.G;
-                const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + r) % P.G;
-                *(uint2*)(P.out + orow * 128 + 4 * lane) =
-                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
             }
         }
         __syncwarp();
