@@ -133,26 +133,35 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         bool ok = true;
         int issued = 0;
-        // One batch = one page per stage (NS <= 32 pages, lane j owns stage
-        // s(j)); the lanes wait for their own stages and issue their copies
-        // together -- one lane issuing every copy in turn caps the staging
-        // rate well below HBM's.  The next batch's page ids are loaded while
-        // this one is issued.
+        // Pages go out in order.  Lane j looks at page i + j: the run of
+        // consecutive pages whose stages are already free is issued in one
+        // instruction (one lane per page; one lane issuing every copy in turn
+        // caps the staging rate well below HBM's); when the next page's stage
+        // is still in use, lane 0 waits for it.  Page ids are loaded 32 at a
+        // time, the next batch while this one is issued.
         const int NS = P.KW * SG;
-        const int jj_l = lane / P.KW;
-        const int s_l = (lane % P.KW) * SG + jj_l % SG;   // stage of lane's page in every batch
-        int next = (lane < NS && lane < n_pages) ? bt[lane] : 0;
-        for (int base = 0; base < n_pages; base += NS) {
-            const int phys = next;
-            if (base + NS < n_pages) next = (lane < NS && base + NS + lane < n_pages) ? bt[base + NS + lane] : 0;
-            const int use = base / NS;
-            const bool mine = lane < NS && base + lane < n_pages;
-            bool okl = true;
-            if (mine) {
-                if (use > 0) okl = mbar_wait(smem_u32(&bars[S + s_l]), (use - 1) & 1);
-                if (okl) {
-                    const uint32_t full = smem_u32(&bars[s_l]);
-                    const uint32_t dk = smem_u32(smem + s_l * C::kStageBytes);
+        int next = (lane < n_pages) ? bt[lane] : 0;
+        for (int base = 0; base < n_pages && ok; base += 32) {
+            const int mine = next;
+            if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
+            const int end = min(n_pages, base + 32);
+            while (issued < end) {
+                const int pj = issued + lane;
+                const int jj = pj / P.KW, use = jj / SG, s = (pj % P.KW) * SG + jj % SG;
+                const bool free = pj < end && (use == 0 || mbar_test(smem_u32(&bars[S + s]), (use - 1) & 1));
+                const unsigned fm = __ballot_sync(0xffffffffu, free);
+                int run = (fm == 0xffffffffu) ? 32 : __ffs(~fm) - 1;
+                if (run == 0) {
+                    if (lane == 0) ok = mbar_wait(smem_u32(&bars[S + s]), (use - 1) & 1);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    run = 1;
+                }
+                run = min(run, NS);
+                const int phys = __shfl_sync(0xffffffffu, mine, (pj - base) & 31);
+                if (lane < run) {
+                    const uint32_t full = smem_u32(&bars[s]);
+                    const uint32_t dk = smem_u32(smem + s * C::kStageBytes);
                     const uint32_t dv = dk + C::kTileBytes;
                     mbar_expect_tx(full, C::kStageBytes);
                     if (FP8) {
@@ -165,10 +174,9 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
                         tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
                     }
                 }
+                __syncwarp();
+                issued += run;
             }
-            ok = __all_sync(0xffffffffu, okl);
-            if (!ok) break;
-            issued = min(n_pages, base + NS);
         }
         // Do not leave while copies into this CTA's shared memory are in flight.
         if (lane == 0) {

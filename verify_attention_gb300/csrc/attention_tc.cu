@@ -176,6 +176,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             prefetch_tensormap(&tm_v);
         }
     }
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tmem = *tmem_slot;
     if (warp == 1 && lane == 0) {
         // L2 prefetch of the block-table entries this partition will read,
         // located from a read of the sequence length made before the wait for
@@ -195,10 +199,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
         }
     }
-    fence_before();
-    __syncthreads();
-    fence_after();
-    const uint32_t tmem = *tmem_slot;
 
     pdl_wait();
     const int L = P.seq_lens[b];
@@ -682,54 +682,40 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
             const float vsc = *P.v_scale;
             const int hh = lane >> 4;                       // staged half row of these dims
-            const int stride = P.cluster * WARPS;
-            // rows r and r + stride together: every remote load of both rows
-            // first (one round trip), then the arithmetic
-            for (int r = split + P.cluster * warp; r < RL; r += 2 * stride) {
-                const int rows[2] = {r, r + stride};
-                uint2 v[2][8];
-                float mp[2], lp[2];
+            for (int r = split + P.cluster * warp; r < RL; r += P.cluster * WARPS) {
+                // every remote load of the row first (one round trip), then the arithmetic
+                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 8;
+                uint2 v[8];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int rq = min(rows[q], RL - 1);
-                    const uint8_t* src = stg + (hh * 128 + rq) * EPI_STRIDE + (lane & 15) * 8;
-#pragma unroll
-                    for (int p = 0; p < 8; ++p)
-                        v[q][p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
-                    mp[q] = -INFINITY;
-                    lp[q] = 0.f;
-                    if (lane < nsplit_b) {
-                        mp[q] = ld_dsmem_f32(dsmem_addr(&xch[rq], lane));
-                        lp[q] = ld_dsmem_f32(dsmem_addr(&xch[128 + rq], lane));
-                    }
+                for (int p = 0; p < 8; ++p) v[p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
+                float mp = -INFINITY, lp = 0.f;
+                if (lane < nsplit_b) {
+                    mp = ld_dsmem_f32(dsmem_addr(&xch[r], lane));
+                    lp = ld_dsmem_f32(dsmem_addr(&xch[128 + r], lane));
                 }
+                float mstar = mp;
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    if (rows[q] >= RL) break;
-                    float mstar = mp[q];
+                for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+                // partition weight 2^(m_p - m*) l_p on its normalised partial
+                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar) * lp;
+                float lsum = w;
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-                    // partition weight 2^(m_p - m*) l_p on its normalised partial
-                    const float w = (mp[q] == -INFINITY) ? 0.f : ex2(mp[q] - mstar) * lp[q];
-                    float lsum = w;
+                for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int p = 0; p < 8; ++p) {
-                        const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
-                        const float2 a = f16x2_to_f32x2(v[q][p].x), c2 = f16x2_to_f32x2(v[q][p].y);
-                        acc.x = fmaf(wp, a.x, acc.x);
-                        acc.y = fmaf(wp, a.y, acc.y);
-                        acc.z = fmaf(wp, c2.x, acc.z);
-                        acc.w = fmaf(wp, c2.y, acc.w);
-                    }
-                    const float inv = vsc / lsum;
-                    const int m = (R0 + rows[q]) / P.G;
-                    const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + rows[q]) % P.G;
-                    *(uint2*)(P.out + orow * 128 + 4 * lane) =
-                        make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+                for (int p = 0; p < 8; ++p) {
+                    const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
+                    const float2 a = f16x2_to_f32x2(v[p].x), c2 = f16x2_to_f32x2(v[p].y);
+                    acc.x = fmaf(wp, a.x, acc.x);
+                    acc.y = fmaf(wp, a.y, acc.y);
+                    acc.z = fmaf(wp, c2.x, acc.z);
+                    acc.w = fmaf(wp, c2.y, acc.w);
                 }
+                const float inv = vsc / lsum;
+                const int m = (R0 + r) / P.G;
+                const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + r) % P.G;
+                *(uint2*)(P.out + orow * 128 + 4 * lane) =
+                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
             }
         }
         __syncwarp();

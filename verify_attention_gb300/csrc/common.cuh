@@ -199,6 +199,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase, uint64_t
     }
 }
 
+// Non-blocking test: has the phase with parity `phase` of an mbarrier completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
 // 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z,
                                             uint32_t bar, uint64_t policy) {
