@@ -57,7 +57,7 @@ def peaks():
 # sources it was built from; a changed source makes the figure stale (None).
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "ncu_attention_tc_verify_global.md")
 KERNEL_SOURCES = ["verify_attention_gb300/csrc/attention_tc.cu", "verify_attention_gb300/csrc/attention.cuh",
-                  "verify_attention_gb300/csrc/common.cuh", "verify_attention_gb300/csrc/tcgen05_tmem.cuh"]
+                  "verify_attention_gb300/csrc/common.cuh", "verify_attention_gb300/csrc/tcgen05.cuh"]
 
 
 def kernel_sources_sha256():
@@ -678,6 +678,47 @@ def cpu_baseline(name, page_size, target_s=12.0):
             "sample": s.describe(n) + f"; host has {os.cpu_count()} cores"}
 
 
+# ------------------------------------------------ the step in one launch
+
+def one_launch_step(w: Workload, stream, steps, warmup, per_layer_step_s, hbm_peak):
+    """The same verify step through fp8kv_paged_attention_layers: all 48
+    layers' append + attention in one persistent launch (layer order kept),
+    one prepared call per cache copy, each captured in a CUDA graph; timed
+    like the per-layer step (same steps, same rotation over cache copies)."""
+    from verify_attention_gb300 import fp8kv
+    calls = []
+    for copy in w.copies:
+        layers = []
+        for l in copy:
+            B, M, Hq, D = l.q.shape
+            layers.append(dict(q=l.q, k_new=l.k_new.view(B, M, -1, D), v_new=l.v_new.view(B, M, -1, D),
+                               k_cache=l.kc, v_cache=l.vc, block_table=l.bt, seq_lens=l.sl,
+                               max_seq_len=l.max_seq_len, k_scale=l.ks, v_scale=l.vs, sm_scale=l.case.sm_scale,
+                               window_left=l.window_left, out=l.out))
+        calls.append(fp8kv.PagedAttentionLayers(layers))
+    with torch.cuda.stream(stream):
+        for c in calls:
+            c(stream)
+    torch.cuda.synchronize()
+    graphs = []
+    n0 = fp8kv.fp8kv_launch_count()
+    for c in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            c(stream)
+        graphs.append(g)
+    launches = (fp8kv.fp8kv_launch_count() - n0) // len(calls)
+    dispatch = fp8kv.fp8kv_last_dispatch()
+    secs = time_graphs(graphs, steps, warmup, stream) / steps
+    status = fp8kv.fp8kv_device_status(clear=True)
+    b = w.bytes_per_step()
+    return {"ms_per_step": secs * 1e3, "verify_steps_per_s": 1 / secs, "gbs": b / secs / 1e9,
+            "frac_of_hbm": b / secs / 1e9 / hbm_peak, "launches_per_step": launches,
+            "speedup_over_per_layer_calls": per_layer_step_s / secs, "device_status": status,
+            "dispatch": dispatch,
+            "entry": "fp8kv_paged_attention_layers (one persistent cooperative launch per step)"}
+
+
 # ------------------------------------------------------ side measurements
 
 def _step_time(w, stream, steps=10, warmup=3):
@@ -943,6 +984,8 @@ def main():
             ls = layers_of_kind(w, wl)
             secs, disp = time_attention_calls(ls, stream, w.ws)
             line["attention_calls"][kind] = call_record(ls[0], secs, disp, hbm_peak)
+    if args.workload == "verify48":
+        line["one_launch"] = one_launch_step(w, stream, args.steps, args.warmup, step_s, hbm_peak)
     if rank == 0 and args.workload == "verify48" and not args.no_extra:
         del graphs
         line.update(side_measurements(dev, stream, hbm_peak, bf16_peak))

@@ -234,6 +234,72 @@ int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const voi
                                  size_t workspace_bytes, void* out, void* stream);
 
 /*
+ * fp8kv_paged_attention_layers -- the verifier step of several layers in one
+ * launch: for each layer in order, fp8kv_append_paged_attention (or, with
+ * k_new = v_new = NULL, fp8kv_paged_attention) with the same results
+ * ("Laguna S 2.1 B70 campaign transfer ledger", table "Result progression",
+ * rows on graph coverage and persistent attention metadata; "Laguna S 2.1
+ * INT4 -- calibrated FP8 KV on Intel B70", section "Contract": the width-12
+ * verifier over the FP8 cache).
+ *
+ * One persistent, cooperative launch with one CTA per SM.  Layer order is
+ * kept: a layer's queries and new tokens are read only after every output row
+ * of the previous layer has been written, as if the previous layer's output
+ * produced them.  The pages of the earlier context are loaded ahead, across
+ * layer boundaries.  Partitions of a sequence's keys combine through the
+ * workspace (normalised f16 partials in E4M3 code units and fp32 (max, sum),
+ * as the cluster combine of fp8kv_paged_attention), so results equal those of
+ * the per-layer calls within the attention tolerance, not bit for bit.
+ *
+ *   layers     (host) n_layers descriptors (1 .. 64), each naming one layer's
+ *              tensors with the meaning, layout and dtype they have in
+ *              fp8kv_append_paged_attention: q, k_new, v_new (device, bf16,
+ *              k_new/v_new may both be NULL), k_cache, v_cache (device, E4M3),
+ *              block_table, seq_lens (device, int32), k_scale, v_scale
+ *              (device fp32), out (device bf16), and host sizes
+ *              max_pages_per_seq, max_seq_len, num_pages, window_left,
+ *              sm_scale.  Layers may share or have their own tensors.
+ *   B, M, Hq, Hkv, D, page_size, cache_dtype: as fp8kv_paged_attention, the
+ *              same for every layer.
+ *   workspace  (device) >= fp8kv_paged_attention_layers_workspace_size bytes,
+ *              16-byte aligned.  Its first bytes hold the launch's
+ *              synchronisation counters: they must be zero before the first
+ *              call on a workspace (cudaMemset once) and every call leaves
+ *              them zero.  Calls sharing a workspace must not overlap on the
+ *              GPU.
+ * Supported: E4M3 cache, D = 128, page_size 32 or 64, 16 < M*Hq/Hkv <= 128
+ * (one 128-row tile of verifier rows per KV head), B*Hkv <= the number of
+ * SMs; other shapes return FP8KV_ERR_UNSUPPORTED.  Per-layer arguments are
+ * validated as in fp8kv_paged_attention before anything is launched.
+ * Device checks as fp8kv_paged_attention; a wait that runs out (2 s) sets
+ * FP8KV_DEV_WAIT_TIMEOUT and the launch still ends.
+ */
+typedef struct {
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    void* k_cache;
+    void* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const float* k_scale;
+    const float* v_scale;
+    void* out;
+    int max_pages_per_seq;
+    int max_seq_len;
+    int num_pages;
+    int window_left;
+    float sm_scale;
+} fp8kv_layer;
+
+/* Workspace bytes of fp8kv_paged_attention_layers; (size_t)-1 on bad arguments. */
+size_t fp8kv_paged_attention_layers_workspace_size(int n_layers, int B, int M, int Hq, int Hkv);
+
+int fp8kv_paged_attention_layers(const fp8kv_layer* layers, int n_layers, int B, int M, int Hq, int Hkv,
+                                 int D, int page_size, int cache_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * fp8kv_paged_attention_noalloc -- fp8kv_paged_attention without a
  * caller-provided workspace.  (The pages have no counterpart: this is an
  * integration convenience, not part of the method.)

@@ -208,3 +208,36 @@ def test_binding_rejects_cpu_tensors():
         fp8kv.fp8kv_cache_insert(k, k, torch.zeros(1, dtype=torch.int64), None, None,
                                  torch.zeros(1, 8, 32, 128, dtype=torch.uint8),
                                  torch.zeros(1, 8, 32, 128, dtype=torch.uint8))
+
+
+def _layer(**over):
+    a = dict(q=P16, k_new=P16, v_new=P16, k_cache=P16, v_cache=P16, block_table=P16, seq_lens=P16, k_scale=P16,
+             v_scale=P16, out=P16, max_pages_per_seq=4, max_seq_len=100, num_pages=16, window_left=-1,
+             sm_scale=0.088)
+    a.update(over)
+    return fp8kv.fp8kv_layer(*a.values())
+
+
+def _layers(L, layers, B=1, M=12, Hq=72, Hkv=8, D=128, ps=32, dt=0, ws=P16, wsb=1 << 30):
+    arr = (fp8kv.fp8kv_layer * len(layers))(*layers)
+    return L.fp8kv_paged_attention_layers(ctypes.byref(arr), len(layers), B, M, Hq, Hkv, D, ps, dt, ws, wsb, NULL)
+
+
+def test_layers_entry_validation_needs_no_device(L):
+    """fp8kv_paged_attention_layers rejects bad arguments before any CUDA call."""
+    ok = _layer()
+    assert _layers(L, [ok, _layer(q=NULL)]) == 1                     # null pointer
+    assert _layers(L, [_layer(k_new=NULL)]) == 1                     # k_new without v_new
+    assert _layers(L, [_layer(out=ctypes.c_void_p((1 << 20) + 8))]) == 1   # misaligned
+    assert _layers(L, [_layer(max_seq_len=200)]) == 1                # beyond the block-table row
+    assert _layers(L, [ok], dt=1) == 2                               # BF16 cache: not this path
+    assert _layers(L, [ok], M=1) == 2                                # 9 rows per KV head: decode shape
+    assert _layers(L, [ok], M=16) == 2                               # 144 rows: two row tiles
+    assert _layers(L, [ok], ps=16) == 2
+    assert _layers(L, [ok], wsb=100) == 3                            # workspace too small
+    assert _layers(L, [ok], ws=NULL) == 3
+    assert _layers(L, [ok], B=0) == 0                                # nothing to do
+    assert L.fp8kv_paged_attention_layers(None, 1, 1, 12, 72, 8, 128, 32, 0, P16, 1 << 30, NULL) == 1
+    need = fp8kv.fp8kv_paged_attention_layers_workspace_size(48, 1, 12, 72, 8)
+    rows = 12 * 72
+    assert need >= rows * 16 * (128 * 2 + 8) and need < rows * 16 * (128 * 2 + 8) + 4096

@@ -65,7 +65,7 @@ extern "C" int fp8kv_device_status(unsigned int* status, int clear) {
     if (cudaDeviceSynchronize() != cudaSuccess) return FP8KV_ERR_CUDA;
     unsigned int s = 0;
     if (fp8kv::status_insert(&s, clear) || fp8kv::status_attention(&s, clear) ||
-        fp8kv::status_attention_tc(&s, clear))
+        fp8kv::status_attention_tc(&s, clear) || fp8kv::status_attention_layers(&s, clear))
         return FP8KV_ERR_CUDA;
     *status = s;
     return FP8KV_OK;

@@ -133,54 +133,43 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
         const int32_t* bt = P.block_table + (int64_t)b * P.mpps + page_begin;
         bool ok = true;
         int issued = 0;
-        // Pages go out in order.  Lane j looks at page i + j: the run of
-        // consecutive pages whose stages are already free is issued in one
-        // instruction (one lane per page; one lane issuing every copy in turn
-        // caps the staging rate well below HBM's); when the next page's stage
-        // is still in use, lane 0 waits for it.  Page ids are loaded 32 at a
-        // time, the next batch while this one is issued.
-        const int NS = P.KW * SG;
+        // page ids 32 at a time, the next batch loaded while this one is issued
         int next = (lane < n_pages) ? bt[lane] : 0;
         for (int base = 0; base < n_pages && ok; base += 32) {
             const int mine = next;
             if (base + 32 < n_pages) next = (base + 32 + lane < n_pages) ? bt[base + 32 + lane] : 0;
-            const int end = min(n_pages, base + 32);
-            while (issued < end) {
-                const int pj = issued + lane;
-                const int jj = pj / P.KW, use = jj / SG, s = (pj % P.KW) * SG + jj % SG;
-                const bool free = pj < end && (use == 0 || mbar_test(smem_u32(&bars[S + s]), (use - 1) & 1));
-                const unsigned fm = __ballot_sync(0xffffffffu, free);
-                int run = (fm == 0xffffffffu) ? 32 : __ffs(~fm) - 1;
-                if (run == 0) {
-                    if (lane == 0) ok = mbar_wait(smem_u32(&bars[S + s]), (use - 1) & 1);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    run = 1;
-                }
-                run = min(run, NS);
-                const int phys = __shfl_sync(0xffffffffu, mine, (pj - base) & 31);
-                if (lane < run) {
-                    const uint32_t full = smem_u32(&bars[s]);
-                    const uint32_t dk = smem_u32(smem + s * C::kStageBytes);
-                    const uint32_t dv = dk + C::kTileBytes;
-                    mbar_expect_tx(full, C::kStageBytes);
-                    if (FP8) {
-                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
-                        tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
-                    } else {
-                        tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
-                        tma_load_3d(dk + PS * 128, &tm_k, 64, hk * PS, phys, full, policy);
-                        tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
-                        tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
+            const int cnt = min(32, n_pages - base);
+            for (int j = 0; j < cnt; ++j) {
+                const int phys = __shfl_sync(0xffffffffu, mine, j);
+                const int i = base + j;
+                const int jj = i / P.KW, use = jj / SG;
+                const int s = (i % P.KW) * SG + jj % SG;
+                if (lane == 0) {
+                    if (use > 0) ok = mbar_wait(smem_u32(&bars[S + s]), (use - 1) & 1);
+                    if (ok) {
+                        const uint32_t full = smem_u32(&bars[s]);
+                        const uint32_t dk = smem_u32(smem + s * C::kStageBytes);
+                        const uint32_t dv = dk + C::kTileBytes;
+                        mbar_expect_tx(full, C::kStageBytes);
+                        if (FP8) {
+                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                        } else {
+                            tma_load_3d(dk, &tm_k, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dk + PS * 128, &tm_k, 64, hk * PS, phys, full, policy);
+                            tma_load_3d(dv, &tm_v, 0, hk * PS, phys, full, policy);
+                            tma_load_3d(dv + PS * 128, &tm_v, 64, hk * PS, phys, full, policy);
+                        }
                     }
                 }
-                __syncwarp();
-                issued += run;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                ++issued;
             }
         }
         // Do not leave while copies into this CTA's shared memory are in flight.
         if (lane == 0) {
-            for (int i = max(0, issued - NS); i < issued; ++i) {
+            for (int i = max(0, issued - P.KW * SG); i < issued; ++i) {
                 const int jj = i / P.KW;
                 mbar_wait(smem_u32(&bars[(i % P.KW) * SG + jj % SG]), (jj / SG) & 1);
             }
@@ -685,7 +674,7 @@ struct MapKey {
     }
 };
 
-static bool cached_cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int num_pages) {
+bool cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int num_pages) {
     constexpr int kSlots = 512;
     struct Entry {
         MapKey key;
@@ -888,8 +877,8 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     if (need && (!workspace || workspace_bytes < need || !al16(workspace))) return FP8KV_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
-    if (!cached_cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||
-        !cached_cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
+    if (!cache_map(&tk, k_cache, fp8, Hkv, page_size, num_pages) ||
+        !cache_map(&tv, v_cache, fp8, Hkv, page_size, num_pages))
         return FP8KV_ERR_CUDA;
 
     AttnParams P = {};
@@ -929,7 +918,6 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
         while (kw * sg * stage_bytes < merge) ++sg;
         P.KW = kw;
         P.SG = sg;
-        if (kw * sg > 32) return FP8KV_ERR_UNSUPPORTED;   // the producer gives each lane one stage
     }
     P.window_left = window_left;
     P.split_pages = plan.split_pages;

@@ -34,6 +34,43 @@ struct AttnParams {
     int num_pages;
 };
 
+// ------------------------------------------------ persistent multi-layer step
+// (attention_layers.cu): one launch runs the append + attention of several
+// layers, layer after layer.
+constexpr int kMaxLayers = 64;          // layers per launch (kernel parameter space)
+constexpr int kLayersMaxSplits = 16;    // partitions per (sequence, KV head)
+
+struct LayerDesc {                      // 64-byte aligned by its tensor maps
+    CUtensorMap tm_k, tm_v;             // 3-D maps of the layer's caches
+    const uint16_t* q;                  // bf16 [B][M][Hq][128]
+    const uint16_t* k_new;              // bf16 [B][M][Hkv][128], or null (no append)
+    const uint16_t* v_new;
+    uint8_t* k_cache;                   // E4M3 [num_pages][Hkv][page_size][128]
+    uint8_t* v_cache;
+    const int32_t* block_table;         // [B][mpps]
+    const int32_t* seq_lens;            // [B]
+    const float* k_scale;
+    const float* v_scale;
+    uint16_t* out;                      // bf16 [B][M][Hq][128]
+    float sm_scale;
+    int mpps, max_seq_len, num_pages, window_left, split_pages, num_splits;
+};
+
+struct LayersParams {
+    int n_layers, B, M, Hq, Hkv, G, R, max_splits;
+    unsigned* counters;                 // [n_layers][B*Hkv] groups, [n_layers] layers, exit
+    uint16_t* part_o;                   // f16 [B*M*Hq][max_splits][128]: partial O / l
+    float* part_ml;                     // [B*M*Hq][max_splits][2]: (max, sum)
+    LayerDesc layer[kMaxLayers];
+};
+
+int launch_attention_layers(const LayersParams& P, int page_size, int grid, cudaStream_t s);
+int layers_max_grid();                  // CTAs of the persistent kernel resident at once
+int status_attention_layers(unsigned int* s, int clear);
+
+// The cached 3-D tensor map of a [num_pages][Hkv][PS][128] cache (attention.cu).
+bool cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int num_pages);
+
 // Append kernel (insert.cu): the same encoding for the other attention paths.
 int launch_append(const void* k, const void* v, const int32_t* seq_lens, const int32_t* block_table, int mpps, int B,
                   int M, int Hkv, const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,

@@ -56,6 +56,10 @@ def lib() -> ctypes.CDLL:
         L.fp8kv_paged_attention_noalloc.restype = i32
         L.fp8kv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                                     i32, i32, i32, vp, vp, f32, i32, i32, vp, vp]
+        L.fp8kv_paged_attention_layers_workspace_size.restype = sz
+        L.fp8kv_paged_attention_layers_workspace_size.argtypes = [i32] * 5
+        L.fp8kv_paged_attention_layers.restype = i32
+        L.fp8kv_paged_attention_layers.argtypes = [vp, i32, i32, i32, i32, i32, i32, i32, i32, vp, sz, vp]
         L.fp8kv_e4m3_encode_bits.restype = i32
         L.fp8kv_e4m3_encode_bits.argtypes = [u32, sz, vp, vp]
         L.fp8kv_selftest_bounded_wait.restype = i32
@@ -239,6 +243,87 @@ def fp8kv_paged_attention_noalloc(q, k_cache, v_cache, block_table, seq_lens, ma
         _stream(stream))
     _check("fp8kv_paged_attention_noalloc", rc)
     return out
+
+
+class fp8kv_layer(ctypes.Structure):
+    """One layer of fp8kv_paged_attention_layers (include/fp8kv.h)."""
+    _fields_ = [("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+                ("seq_lens", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int), ("max_seq_len", ctypes.c_int),
+                ("num_pages", ctypes.c_int), ("window_left", ctypes.c_int), ("sm_scale", ctypes.c_float)]
+
+
+def fp8kv_paged_attention_layers_workspace_size(n_layers, B, M, Hq, Hkv) -> int:
+    n = lib().fp8kv_paged_attention_layers_workspace_size(n_layers, B, M, Hq, Hkv)
+    if n == ctypes.c_size_t(-1).value:
+        raise ValueError("fp8kv_paged_attention_layers_workspace_size: bad arguments")
+    return n
+
+
+class PagedAttentionLayers:
+    """A prepared fp8kv_paged_attention_layers call over fixed tensors (the
+    layers' persistent caches, metadata and buffers): the descriptors are
+    marshalled once; each call passes them, the workspace and the stream.
+
+    layers: dicts with q, k_new, v_new (or None), k_cache, v_cache,
+    block_table, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+    window_left, out -- the arguments of fp8kv_append_paged_attention."""
+
+    def __init__(self, layers, workspace=None):
+        if not layers:
+            raise ValueError("no layers")
+        q0 = layers[0]["q"]
+        B, M, Hq, D = q0.shape
+        P0, Hkv, page_size, _ = layers[0]["k_cache"].shape
+        self.shape = (B, M, Hq, Hkv, D, page_size)
+        arr = (fp8kv_layer * len(layers))()
+        self._keep = []
+        for i, d in enumerate(layers):
+            q, kc, vc = d["q"], d["k_cache"], d["v_cache"]
+            _dev(q, "q", torch.bfloat16), _dev(kc, "k_cache", torch.uint8), _dev(vc, "v_cache", torch.uint8)
+            _dev(d["block_table"], "block_table", torch.int32), _dev(d["seq_lens"], "seq_lens", torch.int32)
+            _dev(d["out"], "out", torch.bfloat16)
+            if tuple(q.shape) != (B, M, Hq, D) or tuple(d["out"].shape) != (B, M, Hq, D):
+                raise ValueError(f"layer {i}: q and out must be {(B, M, Hq, D)}")
+            if tuple(kc.shape[1:]) != (Hkv, page_size, D) or kc.shape != vc.shape:
+                raise ValueError(f"layer {i}: caches must be [pages][{Hkv}][{page_size}][{D}]")
+            kn, vn = d.get("k_new"), d.get("v_new")
+            if (kn is None) != (vn is None):
+                raise ValueError(f"layer {i}: k_new and v_new go together")
+            if kn is not None:
+                for t, n in ((kn, "k_new"), (vn, "v_new")):
+                    _dev(t, n, torch.bfloat16)
+                    if tuple(t.shape) != (B, M, Hkv, D):
+                        raise ValueError(f"layer {i}: {n} must be {(B, M, Hkv, D)}")
+            bt = d["block_table"]
+            arr[i] = fp8kv_layer(_ptr(q), _ptr(kn), _ptr(vn), _ptr(kc), _ptr(vc), _ptr(bt), _ptr(d["seq_lens"]),
+                                 _ptr(d["k_scale"]), _ptr(d["v_scale"]), _ptr(d["out"]), bt.shape[1],
+                                 int(d["max_seq_len"]), int(d.get("num_pages") or kc.shape[0]),
+                                 int(d.get("window_left", -1)), float(d["sm_scale"]))
+            self._keep.append(d)
+        self.layers = arr
+        self.n = len(layers)
+        self.ws_bytes = fp8kv_paged_attention_layers_workspace_size(self.n, B, M, Hq, Hkv)
+        if workspace is None:
+            # the counters at its start must be zero before the first call
+            workspace = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=q0.device)
+        self.workspace = workspace
+
+    def __call__(self, stream=None):
+        B, M, Hq, Hkv, D, page_size = self.shape
+        rc = lib().fp8kv_paged_attention_layers(ctypes.byref(self.layers), self.n, B, M, Hq, Hkv, D, page_size,
+                                                FP8KV_CACHE_E4M3, _ptr(self.workspace), self.workspace.numel(),
+                                                _stream(stream))
+        _check("fp8kv_paged_attention_layers", rc)
+
+
+def fp8kv_paged_attention_layers(layers, workspace=None, stream=None):
+    """Run the verifier step of several layers in one launch (see
+    PagedAttentionLayers); returns the prepared call for reuse."""
+    call = PagedAttentionLayers(layers, workspace)
+    call(stream)
+    return call
 
 
 def fp8kv_e4m3_encode_bits(first: int, n: int, out: torch.Tensor, stream=None):
