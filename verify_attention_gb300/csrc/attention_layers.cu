@@ -80,7 +80,8 @@ enum {
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                     // one per TMEM lane quarter: the two softmax warps
     B_PATCH = B_PAIR + 4,                        // new tokens patched into a staged tile
-    B_COUNT = B_PATCH + 1
+    B_DEP = B_PATCH + 1,                         // converters: the previous layer is complete
+    B_COUNT = B_DEP + 1
 };
 
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
@@ -98,10 +99,10 @@ __device__ __forceinline__ void red_release_add(unsigned* c, unsigned v) {
 __device__ __forceinline__ bool wait_counter(const unsigned* c, unsigned target) {
     if (ld_acquire(c) >= target) return true;
     const uint64_t start = globaltimer();
-    unsigned ns = 32;
+    unsigned ns = 64;
     while (true) {
         __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
+        if (ns < 512) ns <<= 1;
         if (ld_acquire(c) >= target) return true;
         if (globaltimer() - start > 2000000000ull) {
             flag(FP8KV_DEV_WAIT_TIMEOUT);
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
         mbar_init(bar(B_PATCH), CONV_WARPS);
+        mbar_init(bar(B_DEP), 1);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
     } else if (is_converter(warp)) {
         // ---------------------------------------------------------- V widening
         const int ct = converter_index(warp) * 32 + lane;
-        int tg = 0, pi = 0;
+        int tg = 0, pi = 0, di = 0;                         // tiles, patched tiles, dependency waits
         for (int l = 0; l < P.n_layers && ok; ++l) {
             const LayerDesc& D = P.layer[l];
             if (u >= units_of(P, D)) continue;
@@ -357,9 +359,13 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     // this head's new tokens to the cache (the cache-insert
                     // encoding), keeping the first item's codes for the patch
                     if (l > 0) {
-                        bool w = true;
-                        if (lane == 0) w = wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
-                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        // the first converter warp polls, then releases the others
+                        if (ct == 0) {
+                            wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
+                            mbar_arrive(bar(B_DEP));
+                        }
+                        ok = mbar_wait(bar(B_DEP), di & 1);
+                        ++di;
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                     }
                     ksc = *D.k_scale;
@@ -472,10 +478,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
             // the queries depend on the previous layer: wait until all of its
             // units have written their output
             if (l > 0) {
+                // one thread of the CTA polls (many pollers of one counter slow
+                // every access to its memory partition); all eight warps go on,
+                // or all stop (the pairs meet at named barriers)
                 bool w = true;
-                if (lane == 0) w = wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
-                // all eight warps go on, or all stop (the pairs meet at named barriers)
-                ok = soft_all(__shfl_sync(0xffffffffu, w, 0));
+                if (st == 0) w = wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
+                ok = soft_all(w);
                 if (!ok) break;
             }
             const int rr = min(r, RL - 1);
@@ -689,8 +697,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     red_release_add(&grp[(size_t)l * P.B * P.Hkv + g_idx], 1u);
                 }
                 bool w = true;
-                if (lane == 0) w = wait_counter(&grp[(size_t)l * P.B * P.Hkv + g_idx], (unsigned)D.num_splits);
-                ok = __shfl_sync(0xffffffffu, w, 0) && ok;
+                if (st == 0) w = wait_counter(&grp[(size_t)l * P.B * P.Hkv + g_idx], (unsigned)D.num_splits);
+                ok = soft_all(w && ok);
                 if (ok) {
                     // rows split, split + num_splits, ... of the group: one warp per row
                     const float vsc = *D.v_scale;
