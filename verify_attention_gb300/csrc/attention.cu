@@ -523,13 +523,19 @@ __global__ void __maxnreg__(kDecodeRegs) paged_decode_kernel(
 }
 
 // One warp per output row (b, m, h): combine the partitions through their
-// log-sum-exp, O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p.
+// log-sum-exp.  Partials of the mma.sync kernels (F16 = false) are fp32
+// unnormalised O_p * v_scale with (m_p, l_p):
+//     O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p;
+// those of the tensor-memory kernel (F16 = true) are f16 O_p / l_p in E4M3
+// code units: O = v_scale * sum_p w_p O_p / sum_p w_p, w_p = 2^(m_p - m*) l_p.
+template <bool F16>
 __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restrict__ ws_o,
                                                           const float* __restrict__ ws_ml,
                                                           const int32_t* __restrict__ seq_lens, int B, int M,
                                                           int Hq, int G, int tile_rows, int mpps,
                                                           int page_size, int window_left, int split_pages,
-                                                          int num_splits, int max_seq_len, uint16_t* out) {
+                                                          int num_splits, int max_seq_len, const float* v_scale,
+                                                          uint16_t* out) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -550,6 +556,65 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     const float* po = ws_o + row * num_splits * 128 + lane * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
+    if (F16) {
+        const uint16_t* ph = (const uint16_t*)ws_o + row * num_splits * 128 + lane * 4;
+        const float vs = *v_scale;
+        if (ns <= 16) {
+            // every load in flight at once: (max, sum) of partition j on lane j
+            // and this lane's four dims of every partition; then the arithmetic
+            const float2 mlj = lane < ns ? *(const float2*)(ml + 2 * lane) : make_float2(-INFINITY, 0.f);
+            uint2 v[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = u < ns ? *(const uint2*)(ph + (int64_t)u * 128) : make_uint2(0, 0);
+            float mstar = mlj.x;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+            const float w_l = (mlj.x == -INFINITY) ? 0.f : ex2(mlj.x - mstar) * mlj.y;
+            den = w_l;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float w = __shfl_sync(0xffffffffu, w_l, u);       // 0 past ns
+                const float2 a2 = f16x2_to_f32x2(v[u].x), c2 = f16x2_to_f32x2(v[u].y);
+                acc.x = fmaf(w, a2.x, acc.x);
+                acc.y = fmaf(w, a2.y, acc.y);
+                acc.z = fmaf(w, c2.x, acc.z);
+                acc.w = fmaf(w, c2.y, acc.w);
+            }
+        } else {
+            float mstar = -INFINITY;
+            for (int s = lane; s < ns; s += 32) mstar = fmaxf(mstar, ml[2 * s]);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
+            for (int base = 0; base < ns; base += 32) {
+                const int cnt = min(32, ns - base);
+                const float2 mlj =
+                    lane < cnt ? *(const float2*)(ml + 2 * (base + lane)) : make_float2(-INFINITY, 0.f);
+                const float w_l = (mlj.x == -INFINITY) ? 0.f : ex2(mlj.x - mstar) * mlj.y;
+                den += w_l;
+                for (int j = 0; j < cnt; j += 8) {            // eight partial rows in flight
+                    uint2 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        v[u] = j + u < cnt ? *(const uint2*)(ph + (int64_t)(base + j + u) * 128) : make_uint2(0, 0);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float w = __shfl_sync(0xffffffffu, w_l, (j + u) & 31);   // 0 past cnt
+                        const float2 a2 = f16x2_to_f32x2(v[u].x), c2 = f16x2_to_f32x2(v[u].y);
+                        acc.x = fmaf(w, a2.x, acc.x);
+                        acc.y = fmaf(w, a2.y, acc.y);
+                        acc.z = fmaf(w, c2.x, acc.z);
+                        acc.w = fmaf(w, c2.y, acc.w);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        const float f = vs / den;
+        *(uint2*)(out + row * 128 + lane * 4) =
+            make_uint2(pack_bf16x2(acc.x * f, acc.y * f), pack_bf16x2(acc.z * f, acc.w * f));
+        return;
+    }
     if (ns <= 16) {
         // every load in flight at once: lane j's (max, sum) of partition j and
         // this lane's four dims of every partition; then the arithmetic
@@ -951,10 +1016,11 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     if (rc) return rc;
     if (plan.num_splits > 1 && P.cluster <= 1) {
         const int64_t warps = (int64_t)B * M * Hq;
-        cudaError_t e = launch_pdl(attn_reduce_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
-                                   (const float*)P.ws_o, (const float*)P.ws_ml, seq_lens, B, M, Hq, P.G,
-                                   use_tc ? 128 : P.R, max_pages_per_seq, page_size, window_left,
-                                   plan.split_pages, plan.num_splits, max_seq_len, (uint16_t*)out);
+        cudaError_t e = launch_pdl(use_tc ? attn_reduce_kernel<true> : attn_reduce_kernel<false>,
+                                   dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, (const float*)P.ws_o,
+                                   (const float*)P.ws_ml, seq_lens, B, M, Hq, P.G, use_tc ? 128 : P.R,
+                                   max_pages_per_seq, page_size, window_left, plan.split_pages, plan.num_splits,
+                                   max_seq_len, k_scale ? v_scale : nullptr, (uint16_t*)out);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return FP8KV_ERR_CUDA;

@@ -568,11 +568,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const bool direct = nsplit_b == 1;
             const bool combine = !direct && P.cluster > 1;  // partial stays in shared memory
-            // direct: bf16 of O * v_scale / l; workspace partial: fp32 O * v_scale;
-            // cluster partial: f16 of O / l in code units (|x| <= 448, 11-bit
-            // mantissa), half the bytes the other CTAs pull
+            // direct: bf16 of O * v_scale / l; partial (cluster or workspace):
+            // f16 of O / l in code units (|x| <= 448, 11-bit mantissa) beside
+            // its (max, sum), half the bytes of an fp32 partial
             // (a row with no visible key in this partition has l = 0: weight 0, values 0)
-            const float f = direct ? vs / l_tot : (combine ? (l_tot > 0.f ? 1.0f / l_tot : 0.f) : vs);
+            const float f = direct ? vs / l_tot : (l_tot > 0.f ? 1.0f / l_tot : 0.f);
             // This thread's half row (64 dims: bf16 output or fp32 partial)
             // goes through the free staging buffers to one bulk copy: stores
             // straight from the row-per-thread TMEM layout would touch a
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
-                } else if (combine) {
+                } else {
                     uint4* dst = (uint4*)(row_stage + c * 2);
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
@@ -601,12 +601,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
-                } else {
-                    float4* dst = (float4*)(row_stage + c * 4);
-#pragma unroll
-                    for (int v4 = 0; v4 < 8; ++v4)
-                        dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * f, __uint_as_float(ov[4 * v4 + 1]) * f,
-                                              __uint_as_float(ov[4 * v4 + 2]) * f, __uint_as_float(ov[4 * v4 + 3]) * f);
                 }
             }
             if (r < RL && !combine) {
@@ -614,7 +608,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 if (direct)
                     bulk_store(P.out + row_idx * 128 + 64 * half, smem_u32(row_stage), 128);
                 else
-                    bulk_store(P.ws_o + (row_idx * P.num_splits + split) * 128 + 64 * half, smem_u32(row_stage), 256);
+                    bulk_store((uint16_t*)P.ws_o + (row_idx * P.num_splits + split) * 128 + 64 * half,
+                               smem_u32(row_stage), 128);
                 bulk_commit();
                 bulk_wait_read();
             }

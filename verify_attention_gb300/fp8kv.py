@@ -223,6 +223,55 @@ def fp8kv_append_paged_attention(k_new, v_new, q, k_cache, v_cache, block_table,
     return out
 
 
+class PreparedAttention:
+    """fp8kv_append_paged_attention (k_new, v_new given) or
+    fp8kv_paged_attention over fixed tensors, marshalled once: each call
+    passes the prepared arguments and the stream, nothing else.  For serving
+    loops whose caches, metadata and buffers stay at fixed addresses; the
+    tensors must outlive the object."""
+
+    def __init__(self, q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale, sm_scale,
+                 window_left=-1, split_tokens=0, workspace=None, out=None, k_new=None, v_new=None, num_pages=None):
+        dt = _cache_dtype(k_cache)
+        _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache")
+        _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
+        B, M, Hq, D = q.shape
+        P, Hkv, page_size, _ = k_cache.shape
+        if (k_new is None) != (v_new is None):
+            raise ValueError("k_new and v_new go together")
+        if k_new is not None:
+            for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+                _dev(t, n, torch.bfloat16)
+                if tuple(t.shape) != (B, M, Hkv, D):
+                    raise ValueError(f"{n} must be [B][M][Hkv][D]")
+        need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                                    split_tokens)
+        if workspace is None and need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if out is None:
+            out = torch.empty_like(q)
+        if out.shape != q.shape:
+            raise ValueError("out must have the shape of q")
+        self.out, self._keep = out, (q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, workspace, k_new,
+                                     v_new)
+        args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                int(max_seq_len), B, M, Hq, Hkv, D, page_size, int(P if num_pages is None else num_pages),
+                _ptr(k_scale), _ptr(v_scale), float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
+                workspace.numel() if workspace is not None else 0, _ptr(out))
+        if k_new is not None:
+            self._fn, self._name = lib().fp8kv_append_paged_attention, "fp8kv_append_paged_attention"
+            self._args = (_ptr(k_new), _ptr(v_new), *args)
+        else:
+            self._fn, self._name = lib().fp8kv_paged_attention, "fp8kv_paged_attention"
+            self._args = args
+
+    def __call__(self, stream=None):
+        rc = self._fn(*self._args, _stream(stream))
+        if rc:
+            raise Fp8kvError(self._name, rc)
+        return self.out
+
+
 def fp8kv_paged_attention_noalloc(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale,
                                   sm_scale, out, window_left=-1, split_tokens=0, num_pages=None, stream=None):
     """fp8kv_paged_attention with the library's own fixed device workspace, for
