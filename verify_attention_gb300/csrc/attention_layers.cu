@@ -79,8 +79,11 @@ enum {
     B_Q_READY = B_O_FREE + 1,
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                     // one per TMEM lane quarter: the two softmax warps
-    B_PATCH = B_PAIR + 4,                        // new tokens patched into a staged tile
-    B_DEP = B_PATCH + 1,                         // converters: the previous layer is complete
+    // new tokens patched into a staged tile: one barrier for the first and one
+    // for the second of the (at most two) tiles of a unit that hold them, so
+    // that no waiter can fall a whole phase behind
+    B_PATCH = B_PAIR + 4,
+    B_DEP = B_PATCH + 2,                         // converters: the previous layer is complete
     B_COUNT = B_DEP + 1
 };
 
@@ -205,6 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
         mbar_init(bar(B_PATCH), CONV_WARPS);
+        mbar_init(bar(B_PATCH + 1), CONV_WARPS);
         mbar_init(bar(B_DEP), 1);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
@@ -272,7 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         if (lane == 0) {
             constexpr uint32_t ID_QK = idesc(128, NK, false);     // kind::f8f6f4, E4M3 x E4M3
             constexpr uint32_t ID_PV = idesc(128, 128, true);     // kind::f16, V MN-major
-            int tg = 0, qi = 0, pi = 0;                             // tiles, units, patched tiles
+            int tg = 0, qi = 0, pa[2] = {0, 0};                     // tiles, units, uses of each patch barrier
             for (int l = 0; l < P.n_layers && ok; ++l) {
                 const LayerDesc& D = P.layer[l];
                 if (u >= units_of(P, D)) continue;
@@ -284,7 +288,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     if (t < U.n_tiles) {
                         const int g = tg + t, s = g % STAGES, sb = g & 1;
                         ok = mbar_wait(bar(B_STG_FULL + s), (g / STAGES) & 1);
-                        if (ok && t >= U.app_t0 && t <= U.app_t1) ok = mbar_wait(bar(B_PATCH), (pi + t - U.app_t0) & 1);
+                        if (ok && t >= U.app_t0 && t <= U.app_t1)
+                            ok = mbar_wait(bar(B_PATCH + (t - U.app_t0)), pa[t - U.app_t0] & 1);
                         if (!ok) break;
                         fence_after();
                         const uint32_t kt = smem_u32(stg + s * STG_BYTES);
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 }
                 tg += U.n_tiles;
                 ++qi;
-                if (U.app_t1 >= U.app_t0) pi += U.app_t1 - U.app_t0 + 1;
+                for (int k = 0; k <= U.app_t1 - U.app_t0 && k < 2; ++k) ++pa[k];
             }
             // nothing the tensor cores still run may outlive the TMEM allocation
             mma_commit(bar(B_MMA_IDLE));
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
     } else if (is_converter(warp)) {
         // ---------------------------------------------------------- V widening
         const int ct = converter_index(warp) * 32 + lane;
-        int tg = 0, pi = 0, di = 0;                         // tiles, patched tiles, dependency waits
+        int tg = 0, di = 0, pa[2] = {0, 0};                 // tiles, dependency waits, patch-barrier uses
         for (int l = 0; l < P.n_layers && ok; ++l) {
             const LayerDesc& D = P.layer[l];
             if (u >= units_of(P, D)) continue;
@@ -406,9 +411,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     }
                     fence_proxy_async();                    // for the tensor cores' read of K
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_PATCH));
+                    if (lane == 0) mbar_arrive(bar(B_PATCH + (t - U.app_t0)));
                     // every converter warp's rows are in place before V is read
-                    ok = mbar_wait(bar(B_PATCH), (pi + t - U.app_t0) & 1);
+                    ok = mbar_wait(bar(B_PATCH + (t - U.app_t0)), pa[t - U.app_t0] & 1);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 }
                 const int zlo = max(0, min(NK, U.lo0 - k0));
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 }
             }
             tg += U.n_tiles;
-            if (U.app_t1 >= U.app_t0) pi += U.app_t1 - U.app_t0 + 1;
+            for (int k = 0; k <= U.app_t1 - U.app_t0 && k < 2; ++k) ++pa[k];
         }
     } else {
         // ------------------------------------------------------------ softmax

@@ -74,8 +74,11 @@ enum {
     B_Q_READY = B_O_FINAL + 1,
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                    // one per TMEM lane quarter: the two softmax warps
-    B_PATCH = B_PAIR + 4,                       // append: new tokens patched into the staged tile
-    B_COUNT = B_PATCH + 1
+    // append: new tokens patched into a staged tile, one barrier for each of
+    // the (at most two) tiles that hold them, so that no waiter can fall a
+    // whole phase behind
+    B_PATCH = B_PAIR + 4,
+    B_COUNT = B_PATCH + 2
 };
 
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
         mbar_init(bar(B_PATCH), CONV_WARPS);
+        mbar_init(bar(B_PATCH + 1), CONV_WARPS);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 if (t < n_tiles) {
                     const int s = t % STAGES, sb = t & 1;
                     ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);
-                    if (ok && t >= app_t0 && t <= app_t1) ok = mbar_wait(bar(B_PATCH), (t - app_t0) & 1);
+                    if (ok && t >= app_t0 && t <= app_t1) ok = mbar_wait(bar(B_PATCH + (t - app_t0)), 0);
                     if (!ok) break;
                     fence_after();
                     const uint32_t kt = smem_u32(stg + s * STG_BYTES);
@@ -345,9 +349,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 }
                 fence_proxy_async();                        // for the tensor cores' read of K
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_PATCH));
+                if (lane == 0) mbar_arrive(bar(B_PATCH + (t - app_t0)));
                 // every converter warp's rows are in place before V is read
-                ok = mbar_wait(bar(B_PATCH), (t - app_t0) & 1);
+                ok = mbar_wait(bar(B_PATCH + (t - app_t0)), 0);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             }
             const int pages_here = min(PPT, n_pages - t * PPT);
