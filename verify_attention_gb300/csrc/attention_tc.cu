@@ -50,10 +50,15 @@ constexpr int NK = 128;                         // keys per tile
 constexpr int STAGES = 3;                       // E4M3 staging tiles (K + V)
 constexpr int STG_K = NK * 128;                 // 16 KiB
 constexpr int STG_BYTES = 2 * STG_K;            // 32 KiB
-constexpr int VBUFS = 3;                        // f16 V tiles
+constexpr int VBUFS = 2;                        // f16 V tiles
 constexpr int VBUF_BYTES = NK * 256;            // 32 KiB
 constexpr int XCH_BYTES = 3 * 2 * 128 * 4;      // [tile parity 0, parity 1, row sums][half][row]
-constexpr int SMEM = STAGES * STG_BYTES + VBUFS * VBUF_BYTES + XCH_BYTES + 1024 + 512;
+// Cluster combine: the partials a CTA receives for the rows it owns (row r
+// belongs to rank r mod C): C partitions x ceil(rows / C) slots, an f16 row
+// (O / l, 128 dims) and fp32 (max, sum) each; at most 136 slots for C <= 8.
+constexpr int RECV_SLOTS = 136;
+constexpr int RECV_BYTES = RECV_SLOTS * (256 + 8);
+constexpr int SMEM = STAGES * STG_BYTES + VBUFS * VBUF_BYTES + XCH_BYTES + RECV_BYTES + 1024 + 512;
 // epilogue: one staged half row (<= 256 B) per (half, row), padded against
 // bank conflicts, in the staging buffers (free once the last tile is consumed)
 constexpr int EPI_STRIDE = 272;
@@ -94,7 +99,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     uint8_t* stg = smem;                                    // STAGES x (K 16 KiB, V 16 KiB)
     uint8_t* vbuf = smem + STAGES * STG_BYTES;              // VBUFS x 32 KiB
     float* xch = (float*)(vbuf + VBUFS * VBUF_BYTES);       // [parity][half][row]
-    uint64_t* bars = (uint64_t*)((uint8_t*)xch + XCH_BYTES);
+    uint8_t* recv = (uint8_t*)xch + XCH_BYTES;              // [partition][slot] f16 rows
+    float* recv_ml = (float*)(recv + RECV_SLOTS * 256);     // [partition][slot] (max, sum)
+    uint64_t* bars = (uint64_t*)(recv + RECV_BYTES);
     uint32_t* tmem_slot = (uint32_t*)(bars + B_COUNT);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -597,14 +604,29 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
                 } else {
-                    uint4* dst = (uint4*)(row_stage + c * 2);
+                    uint4 w[4];
 #pragma unroll
                     for (int v4 = 0; v4 < 4; ++v4)
-                        dst[v4] = make_uint4(
+                        w[v4] = make_uint4(
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 0]) * f, __uint_as_float(ov[8 * v4 + 1]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 2]) * f, __uint_as_float(ov[8 * v4 + 3]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
+                    if (combine) {
+                        // straight into the receive area of the row's owner
+                        // (rank r mod C), slot r / C of this partition
+                        if (r < RL) {
+                            const int C = P.cluster, slots = (RL + C - 1) / C;
+                            const uint32_t a =
+                                dsmem_addr(recv + (split * slots + r / C) * 256 + half * 128 + c * 2, r % C);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) st_dsmem_u32x4(a + 16 * v4, w[v4]);
+                        }
+                    } else {
+                        uint4* dst = (uint4*)(row_stage + c * 2);
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4) dst[v4] = w[v4];
+                    }
                 }
             }
             if (r < RL && !combine) {
@@ -619,8 +641,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             }
             if (r < RL && !direct && half == 0) {
                 if (combine) {
-                    xch[r] = m_run;                         // the tile exchange area is free now
-                    xch[128 + r] = l_tot;
+                    const int C = P.cluster, slots = (RL + C - 1) / C;
+                    st_dsmem_f32x2(dsmem_addr(recv_ml + (split * slots + r / C) * 2, r % C), m_run, l_tot);
                 } else {
                     P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
                     P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_tot;
@@ -632,30 +654,32 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     if (P.cluster > 1) {
         // ------------------------------------------------- cluster combine
         // The partitions of this (KV head, sequence) are the CTAs of one
-        // cluster (rank = partition): each combines rows rank, rank + C, ...
-        // one warp per row, lane l owning dims 4l..4l+3, reading every
-        // partition's (m, l) and fp32 partial O from its shared memory:
-        // O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p.
+        // cluster (rank = partition).  Each has pushed its partial rows to
+        // their owners (row r to rank r mod C); after one cluster barrier
+        // every CTA combines the rows it owns from its own shared memory,
+        // one warp per row, lane l owning dims 4l..4l+3:
+        // O = v_scale * sum_p w_p O_p / sum_p w_p, w_p = 2^(m_p - m*) l_p.
+        // Nothing is read remotely, so no second barrier is needed.
         __syncwarp();
         cluster_sync_all();
         if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
             const float vsc = *P.v_scale;
-            const int hh = lane >> 4;                       // staged half row of these dims
-            for (int r = split + P.cluster * warp; r < RL; r += P.cluster * WARPS) {
-                // every remote load of the row first (one round trip), then the arithmetic
-                const uint8_t* src = stg + (hh * 128 + r) * EPI_STRIDE + (lane & 15) * 8;
+            const int C = P.cluster, slots = (RL + C - 1) / C;
+            for (int k = warp; k < slots && split + C * k < RL; k += WARPS) {
+                const int r = split + C * k;
                 uint2 v[8];
 #pragma unroll
-                for (int p = 0; p < 8; ++p) v[p] = p < nsplit_b ? ld_dsmem_u32x2(dsmem_addr(src, p)) : make_uint2(0, 0);
+                for (int p = 0; p < 8; ++p)
+                    v[p] = p < nsplit_b ? *(const uint2*)(recv + (p * slots + k) * 256 + lane * 8) : make_uint2(0, 0);
                 float mp = -INFINITY, lp = 0.f;
                 if (lane < nsplit_b) {
-                    mp = ld_dsmem_f32(dsmem_addr(&xch[r], lane));
-                    lp = ld_dsmem_f32(dsmem_addr(&xch[128 + r], lane));
+                    const float2 ml = *(const float2*)(recv_ml + (lane * slots + k) * 2);
+                    mp = ml.x;
+                    lp = ml.y;
                 }
                 float mstar = mp;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-                // partition weight 2^(m_p - m*) l_p on its normalised partial
                 const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar) * lp;
                 float lsum = w;
 #pragma unroll
@@ -677,8 +701,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                     make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
             }
         }
-        __syncwarp();
-        cluster_sync_all();                                 // no CTA leaves while others read it
     }
 
     // ---------------------------------------------------------------- teardown

@@ -309,6 +309,13 @@ __device__ __forceinline__ uint2 ld_dsmem_u32x2(uint32_t a) {
     asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
     return v;
 }
+__device__ __forceinline__ void st_dsmem_u32x4(uint32_t a, uint4 v) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f32x2(uint32_t a, float x, float y) {
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+}
 // Every thread of every CTA of the cluster: writes before it are visible to
 // reads after it anywhere in the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
