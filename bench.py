@@ -258,7 +258,7 @@ def workload_description(name, page_size, cache_dtype="e4m3"):
     return {
         "verify48": (f"48 layers [SW512,SW512,SW512,G]x12, B=1, M=12, Hq=72, Hkv=8, D=128, L=8192, "
                      f"page {page_size}, E4M3 cache; per layer 12-token insert + attention"),
-        "decode128k": (f"12 global layers, B=1, M=1, Hq=72, Hkv=8, D=128, L=131072, page 64, "
+        "decode128k": (f"12 global layers, B=1, M=1, Hq=72, Hkv=8, D=128, L=131072, page {page_size}, "
                        f"{cache_dtype} cache; per layer 1-token insert + split-KV attention + reduce"),
         "prefill16k": ("4 global layers, B=1, a prefill chunk of M=1024 tokens at the end of L=16384, Hq=72, "
                        "Hkv=8, D=128, page 64, E4M3 cache; per layer 1024-token append + causal attention in "
@@ -286,11 +286,11 @@ def build_workload(name, page_size, device, cache_dtype="e4m3", layers=None):
     if name == "decode128k":
         copies = [[]]
         for l in range(layers or 12):
-            c = gen.cfg4_case(l, device=device)
+            c = gen.cfg4_case(l, device=device, page_size=page_size)
             copies[0].append(Layer(c, device, cache_dtype=cache_dtype, split_tokens=0))
             fp = case_sha256(c) if l == 0 else fp
             _free_context([c])
-        return _fingerprinted(Workload(name, copies, workload_description(name, 64, cache_dtype), 1), fp)
+        return _fingerprinted(Workload(name, copies, workload_description(name, page_size, cache_dtype), 1), fp)
     if name == "prefill16k":
         copies = [[]]
         for l in range(layers or 4):
@@ -767,7 +767,8 @@ def side_measurements(dev, stream, hbm_peak, bf16_peak):
     the one JSON line (device time, CUDA-graph replays, caches rotated or
     larger than L2):
       verify48_page64  the 48-layer step at page 64 (the page-size A/B);
-      decode128k       12 long-context decode layers, E4M3 and BF16 cache;
+      decode128k       12 long-context decode layers, E4M3 and BF16 cache at
+                       page 64, E4M3 at page 32;
       prefill16k       a prefill chunk on the tensor cores;
       serving64        the batched serving mix, per layer kind;
       cfg1, cfg2       the single-layer configurations (rotating cache copies)."""
@@ -796,7 +797,15 @@ def side_measurements(dev, stream, hbm_peak, bf16_peak):
                    "attention_ms": t2 * 1e3, "attention_bytes": b2, "dispatch": d2}
         del w
         torch.cuda.empty_cache()
-    out["decode128k"] = {**dec["e4m3"], "bf16": dec["bf16"],
+    w = build_workload("decode128k", 32, dev)
+    s2, _ = _step_time(w, stream, steps=5)
+    b2, t2, _, d2 = dominant_kernel(w, stream, reps=12)
+    dec["e4m3_page32"] = {"gbs_step": w.bytes_per_step() / s2 / 1e9, "ms_per_step": s2 * 1e3,
+                          "attention_gbs": b2 / t2 / 1e9, "attention_frac": b2 / t2 / 1e9 / hbm_peak,
+                          "attention_ms": t2 * 1e3, "attention_bytes": b2, "dispatch": d2}
+    del w
+    torch.cuda.empty_cache()
+    out["decode128k"] = {**dec["e4m3"], "bf16": dec["bf16"], "page32": dec["e4m3_page32"],
                          "fp8_over_bf16_step_speedup": dec["bf16"]["ms_per_step"] / dec["e4m3"]["ms_per_step"],
                          "fp8_over_bf16_attention_speedup": dec["bf16"]["attention_ms"] / dec["e4m3"]["attention_ms"]}
     w = build_workload("prefill16k", 64, dev)

@@ -227,8 +227,8 @@ def cfg3_case(layer: int, page_size: int, device="cpu") -> LayerCase:
                       window=cfg3_layer_kinds()[layer], device=device)
 
 
-def cfg4_case(layer: int, device="cpu", seq_len: int = 131072) -> LayerCase:
-    return layer_case(1004 * 100 + layer, [seq_len], 1, 64, outlier_frac=0.01, device=device)
+def cfg4_case(layer: int, device="cpu", seq_len: int = 131072, page_size: int = 64) -> LayerCase:
+    return layer_case(1004 * 100 + layer, [seq_len], 1, page_size, outlier_frac=0.01, device=device)
 
 
 def cfg5_seq_lens(B: int = 64) -> List[int]:
