@@ -42,6 +42,9 @@ def _declare(L):
     L.oracle_e4m3_encode_bits_range.argtypes = [ctypes.c_uint32, sz, vp]
     L.oracle_cache_insert.restype = i32
     L.oracle_cache_insert.argtypes = [vp, vp, vp, i32, i32, i32, f32, f32, vp, vp, i32, i32, i32]
+    L.oracle_cache_insert_per_head.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32]
+    L.oracle_paged_attention_per_head.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                                  vp, vp, f64, i32, vp]
     L.oracle_rope_table.argtypes = [f64, i32, i32, vp]
     L.oracle_norm_rope_row.restype = i32
     L.oracle_norm_rope_row.argtypes = [vp, vp, f32, vp, i32, vp]
@@ -104,6 +107,25 @@ def cache_insert(k, v, slot_mapping, k_scale, v_scale, k_cache, v_cache, cache_d
                                    num_pages, page_size, cache_dtype)
     if rc:
         raise ValueError("oracle_cache_insert: bad arguments")
+
+
+def cache_insert_per_head(k, v, slot_mapping, k_scales, v_scales, k_cache, v_cache):
+    """Insert bf16 K/V rows ``[T][Hkv][D]`` into E4M3 caches in place, head h
+    encoded with its own scale k_scales[h] (v_scales[h]), fp32."""
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int64)
+    T, Hkv, D = k.shape
+    ks = _c(np.asarray(k_scales, np.float32).reshape(-1), np.float32)
+    vs = _c(np.asarray(v_scales, np.float32).reshape(-1), np.float32)
+    if ks.shape[0] != Hkv or vs.shape[0] != Hkv:
+        raise ValueError("one scale per KV head")
+    num_pages, _, page_size, _ = k_cache.shape
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous and k_cache.dtype == np.uint8
+    rc = lib().oracle_cache_insert_per_head(_p(k), _p(v), _p(slot_mapping), T, Hkv, D, _p(ks), _p(vs),
+                                            _p(k_cache), _p(v_cache), num_pages, page_size)
+    if rc:
+        raise ValueError("oracle_cache_insert_per_head: bad arguments")
 
 
 # ------------------------------------------------------- RMSNorm and RoPE
@@ -193,4 +215,28 @@ def paged_attention_rows(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_
         rc = lib().oracle_paged_attention_rows(*args, _p(rows), rows.shape[0], _p(out))
     if rc:
         raise ValueError("oracle_paged_attention_rows: bad arguments")
+    return out
+
+
+def paged_attention_per_head(q, k_cache, v_cache, block_table, seq_lens, k_scales, v_scales, sm_scale,
+                             window_left=-1):
+    """float64 ``[B][M][Hq][D]`` over an E4M3 cache whose KV head hk is
+    dequantized with k_scales[hk], v_scales[hk]."""
+    q = _c(q, np.uint16)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B, M, Hq, D = q.shape
+    num_pages, Hkv, page_size, _ = k_cache.shape
+    ks = _c(np.asarray(k_scales, np.float64).reshape(-1), np.float64)
+    vs = _c(np.asarray(v_scales, np.float64).reshape(-1), np.float64)
+    if ks.shape[0] != Hkv or vs.shape[0] != Hkv:
+        raise ValueError("one scale per KV head")
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous and k_cache.dtype == np.uint8
+    out = np.empty((B, M, Hq, D), np.float64)
+    rc = lib().oracle_paged_attention_per_head(_p(q), _p(k_cache), _p(v_cache), _p(block_table),
+                                               block_table.shape[1], _p(seq_lens), B, M, Hq, Hkv, D,
+                                               page_size, num_pages, _p(ks), _p(vs), float(sm_scale),
+                                               int(window_left), _p(out))
+    if rc:
+        raise ValueError("oracle_paged_attention_per_head: bad arguments")
     return out

@@ -5,6 +5,8 @@ the parity checks at full workload sizes, where the C oracle's one-element-
 at-a-time loops would take hours:
 
     Kd = decode(k_code) * k_scale,  Vd = decode(v_code) * v_scale
+    (k_scale, v_scale: scalars, or per-head arrays [Hkv] -- an extension the
+    pages do not use -- whose entry hk scales KV head hk)
     out[b][m][h] = softmax_j( (q . Kd_j) * sm_scale ) . Vd      over visible j
 
 "Exact q1/M12 paged attention" over the E4M3 cache ("Laguna S 2.1 INT4 --
@@ -38,6 +40,12 @@ def _bf16_to_f64(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def _scale_of(scale, hk):
+    """A scalar scale, or head hk's entry of per-head scales [Hkv]."""
+    a = np.asarray(scale, np.float64).reshape(-1)
+    return float(a[0] if a.shape[0] == 1 else a[hk])
+
+
 def _rows_of_group(q_bits, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale, sm_scale, b, hk,
                    window_left, cache_dtype, table):
     """float64 [M][G][D]: every query row of KV head hk of sequence b."""
@@ -58,8 +66,8 @@ def _rows_of_group(q_bits, k_cache, v_cache, block_table, seq_lens, k_scale, v_s
     offs = keys % ps
     pg = np.clip(pages, 0, num_pages - 1)        # a row whose keys touch a bad page is refused below
     if cache_dtype == E4M3:
-        kd = table[k_cache[pg, hk, offs, :]] * float(k_scale)           # [n][D]
-        vd = table[v_cache[pg, hk, offs, :]] * float(v_scale)
+        kd = table[k_cache[pg, hk, offs, :]] * _scale_of(k_scale, hk)   # [n][D]
+        vd = table[v_cache[pg, hk, offs, :]] * _scale_of(v_scale, hk)
     else:
         kd = _bf16_to_f64(k_cache[pg, hk, offs, :])
         vd = _bf16_to_f64(v_cache[pg, hk, offs, :])

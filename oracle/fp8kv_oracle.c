@@ -18,6 +18,10 @@
  *    requests": kv_cache_scheme with strategy "tensor", symmetric, dynamic false).
  *    Reading: stored code = E4M3(fp32(x) / scale), round to nearest even,
  *    saturating to +-448.
+ *  - Per-head scales (an extension the pages do not use: the checkpoint asks for
+ *    strategy "tensor"): one scale per KV head for K and one for V, each the
+ *    same kind of static symmetric scalar; every element of head h is encoded
+ *    and decoded with that head's scale, nothing else changes.
  *  - Q/K RMSNorm + RoPE ahead of the insert ("calibrated FP8 KV on Intel B70",
  *    section "Initial optimization order", item 3; ledger table "Result
  *    progression", row "Exact fusion stack").  The pages give no epsilon, no
@@ -160,6 +164,29 @@ int oracle_cache_insert(const uint16_t* k, const uint16_t* v, const int64_t* slo
     return ORACLE_OK;
 }
 
+/* Per-head scales: head h of K (V) is encoded with k_scale[h] (v_scale[h]);
+ * E4M3 cache only. */
+int oracle_cache_insert_per_head(const uint16_t* k, const uint16_t* v, const int64_t* slot_mapping,
+                                 int T, int Hkv, int D, const float* k_scale, const float* v_scale,
+                                 uint8_t* k_cache, uint8_t* v_cache, int num_pages, int page_size)
+{
+    if (T < 0 || Hkv <= 0 || D <= 0 || page_size <= 0 || num_pages < 0) return ORACLE_BAD_ARG;
+    for (int t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0) continue;
+        if (slot >= (int64_t)num_pages * page_size) return ORACLE_BAD_ARG;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int d = 0; d < D; ++d) {
+                size_t src = ((size_t)t * Hkv + h) * D + d;
+                size_t dst = cache_index(slot, h, d, Hkv, page_size, D);
+                k_cache[dst] = oracle_e4m3_encode(bf16_to_f32(k[src]) / k_scale[h]);
+                v_cache[dst] = oracle_e4m3_encode(bf16_to_f32(v[src]) / v_scale[h]);
+            }
+        }
+    }
+    return ORACLE_OK;
+}
+
 /* ------------------------------------------------------ RMSNorm and RoPE */
 
 /* Rotary table, one row per position: cos of the D/2 frequencies, then their
@@ -270,6 +297,8 @@ typedef struct {
     int B, M, Hq, Hkv, D, page_size, num_pages;
     double k_scale, v_scale, sm_scale;
     int window_left;              /* -1: global; else keys j >= p - window_left */
+    const double* k_scale_h;      /* per-head scales [Hkv] (E4M3), or NULL: k_scale, v_scale */
+    const double* v_scale_h;
 } attn_args;
 
 /* Dequantized element d of key/value j (logical position) for kv head hk. */
@@ -304,8 +333,8 @@ static int row_partial(const attn_args* a, int b, int m, int h, int j0, int j1,
     const uint16_t* q = a->q + (((size_t)b * a->M + m) * a->Hq + h) * D;
     for (int d = 0; d < D; ++d) acc[d] = 0.0;
     if (j1 < j0) { *mx_out = -INFINITY; *l_out = 0.0; return 0; }
-    double k_scale = a->cache_dtype == 0 ? a->k_scale : 1.0;
-    double v_scale = a->cache_dtype == 0 ? a->v_scale : 1.0;
+    double k_scale = a->cache_dtype == 0 ? (a->k_scale_h ? a->k_scale_h[hk] : a->k_scale) : 1.0;
+    double v_scale = a->cache_dtype == 0 ? (a->v_scale_h ? a->v_scale_h[hk] : a->v_scale) : 1.0;
     double mx = -INFINITY;
     for (int j = j0; j <= j1; ++j) {
         double dot = 0.0;
@@ -402,7 +431,7 @@ static int attention_rows_impl(const attn_args* a, const int32_t* rows, int n_ro
 #define ATTN_INIT                                                                       \
     attn_args a = {q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq,     \
                    seq_lens, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale,  \
-                   sm_scale, window_left}
+                   sm_scale, window_left, NULL, NULL}
 
 int oracle_paged_attention_rows(ATTN_PARAMS, const int32_t* rows, int n_rows, double* out)
 {
@@ -422,6 +451,31 @@ int oracle_paged_attention_split_rows(ATTN_PARAMS, int split_tokens, const int32
 int oracle_paged_attention(ATTN_PARAMS, double* out)
 {
     ATTN_INIT;
+    size_t n = (size_t)B * M * Hq;
+    int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * 3 * (n ? n : 1));
+    if (!rows) return ORACLE_BAD_ARG;
+    size_t i = 0;
+    for (int b = 0; b < B; ++b)
+        for (int m = 0; m < M; ++m)
+            for (int h = 0; h < Hq; ++h) {
+                rows[3 * i] = b; rows[3 * i + 1] = m; rows[3 * i + 2] = h;
+                ++i;
+            }
+    int rc = attention_rows_impl(&a, rows, (int)n, 0, out);
+    free(rows);
+    return rc;
+}
+
+/* All rows over an E4M3 cache with per-head scales k_scale[Hkv], v_scale[Hkv];
+ * out is [B][M][Hq][D]. */
+int oracle_paged_attention_per_head(const uint16_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                                    const int32_t* block_table, int max_pages_per_seq,
+                                    const int32_t* seq_lens, int B, int M, int Hq, int Hkv, int D,
+                                    int page_size, int num_pages, const double* k_scale,
+                                    const double* v_scale, double sm_scale, int window_left, double* out)
+{
+    attn_args a = {q, k_cache, v_cache, 0, block_table, max_pages_per_seq, seq_lens, B, M, Hq, Hkv, D,
+                   page_size, num_pages, 0.0, 0.0, sm_scale, window_left, k_scale, v_scale};
     size_t n = (size_t)B * M * Hq;
     int32_t* rows = (int32_t*)malloc(sizeof(int32_t) * 3 * (n ? n : 1));
     if (!rows) return ORACLE_BAD_ARG;

@@ -524,6 +524,111 @@ def test_numpy_and_c_attention_agree(seq_lens, M, ps, window):
     assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
 
 
+# ------------------------------------------------------- per-head scales
+# An extension the pages do not use (their checkpoint asks for one scale per
+# tensor, "KV-cache precision decision", "What the official checkpoint
+# requests"): KV head h is encoded and decoded with its own scale.  Pinned by
+# reduction to the per-tensor routines pinned above, head by head, and by a
+# closed form.
+
+def _per_head_case(seed=151, seq_lens=(45, 20), M=5, ps=8, Hq=6, Hkv=3, window=None):
+    case = gen.layer_case(seed, list(seq_lens), M, ps, window=window, Hq=Hq, Hkv=Hkv, k_head_scale=(0.25, 4.0))
+    ks = np.array([0.011, 0.023, 0.047], np.float32)[:Hkv]
+    vs = np.array([0.031, 0.0155, 0.062], np.float32)[:Hkv]
+    return case, ks, vs
+
+
+def _insert_all(case, insert, kc, vc, ks, vs):
+    for kk, vv, ss in ((case.k_prior, case.v_prior, case.slots_prior), (case.k_new, case.v_new, case.slots_new)):
+        insert(gen.bf16_bits(kk), gen.bf16_bits(vv), ss.numpy(), ks, vs, kc, vc)
+
+
+def test_per_head_insert_reduces_to_per_tensor_per_head():
+    case, ks, vs = _per_head_case()
+    P, Hkv = case.layout.num_pages, 3
+    kc = np.full((P, Hkv, 8, 128), 0xA5, np.uint8)
+    vc = kc.copy()
+    _insert_all(case, oracle.cache_insert_per_head, kc, vc, ks, vs)
+    for h in range(Hkv):
+        kt = np.full_like(kc, 0xA5)
+        vt = kt.copy()
+        _insert_all(case, oracle.cache_insert, kt, vt, float(ks[h]), float(vs[h]))
+        assert np.array_equal(kc[:, h], kt[:, h]) and np.array_equal(vc[:, h], vt[:, h]), h
+    # the heads' scales differ, so the heads' bytes must differ from a
+    # single-scale insert somewhere (a scale index dropped would pass above
+    # only for head 0)
+    k0 = np.full_like(kc, 0xA5)
+    v0 = k0.copy()
+    _insert_all(case, oracle.cache_insert, k0, v0, float(ks[0]), float(vs[0]))
+    assert not np.array_equal(kc[:, 1:], k0[:, 1:]) and not np.array_equal(vc[:, 1:], v0[:, 1:])
+
+
+def test_per_head_insert_equal_scales_equal_per_tensor():
+    case, _, _ = _per_head_case(seed=152)
+    P = case.layout.num_pages
+    kc = np.full((P, 3, 8, 128), 0xA5, np.uint8)
+    vc = kc.copy()
+    _insert_all(case, oracle.cache_insert_per_head, kc, vc, np.full(3, 0.02, np.float32), np.full(3, 0.03, np.float32))
+    kt = np.full_like(kc, 0xA5)
+    vt = kt.copy()
+    _insert_all(case, oracle.cache_insert, kt, vt, 0.02, 0.03)
+    assert np.array_equal(kc, kt) and np.array_equal(vc, vt)
+
+
+PER_HEAD_ATTN = {"c": oracle.paged_attention_per_head, "numpy": attention_np.paged_attention}
+
+
+@pytest.mark.parametrize("impl", sorted(PER_HEAD_ATTN))
+@pytest.mark.parametrize("window", [None, 9])
+def test_per_head_attention_reduces_to_per_tensor_per_head(impl, window):
+    case, ks, vs = _per_head_case(seed=153, window=window)
+    P, Hkv, G = case.layout.num_pages, 3, 2
+    kc = np.full((P, Hkv, 8, 128), 0xA5, np.uint8)
+    vc = kc.copy()
+    _insert_all(case, oracle.cache_insert_per_head, kc, vc, ks, vs)
+    q, bt, sl = gen.bf16_bits(case.q), case.layout.block_table.numpy(), case.layout.seq_lens.numpy()
+    out = PER_HEAD_ATTN[impl](q, kc, vc, bt, sl, ks.astype(np.float64), vs.astype(np.float64), case.sm_scale,
+                              window_left=case.window_left)
+    for hk in range(Hkv):
+        ref = oracle.paged_attention(q, kc, vc, bt, sl, float(ks[hk]), float(vs[hk]), case.sm_scale,
+                                     window_left=case.window_left)
+        assert np.allclose(out[:, :, hk * G:(hk + 1) * G], ref[:, :, hk * G:(hk + 1) * G], rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("impl", sorted(PER_HEAD_ATTN))
+def test_per_head_attention_constant_keys_closed_form(impl):
+    """Equal keys in every head: each row returns v_scale[hk] times the mean
+    of its visible V codes' values, for every head's own v_scale."""
+    case, ks, vs = _per_head_case(seed=154)
+    P, Hkv, G, M = case.layout.num_pages, 3, 2, 5
+    kc = np.full((P, Hkv, 8, 128), 0x3A, np.uint8)
+    vc = np.full((P, Hkv, 8, 128), 0xA5, np.uint8)
+    _insert_all(case, oracle.cache_insert_per_head, np.empty_like(kc), vc, ks, vs)
+    out = PER_HEAD_ATTN[impl](gen.bf16_bits(case.q), kc, vc, case.layout.block_table.numpy(),
+                              case.layout.seq_lens.numpy(), ks.astype(np.float64), vs.astype(np.float64),
+                              case.sm_scale)
+    codes = oracle.e4m3_decode(np.arange(256, dtype=np.uint8))
+    bt = case.layout.block_table.numpy()
+    for b, L in enumerate([45, 20]):
+        for m in range(M):
+            p = L - M + m
+            for h in range(6):
+                hk = h // G
+                vals = [codes[vc[bt[b, j // 8], hk, j % 8]] for j in range(0, p + 1)]
+                assert np.allclose(out[b, m, h], float(vs[hk]) * np.mean(vals, axis=0), rtol=1e-12, atol=1e-15)
+
+
+def test_per_head_scales_of_the_generator():
+    """minmax/448 of each head's whole K and V, fp32."""
+    case, _, _ = _per_head_case(seed=155)
+    k = torch.cat([case.k_prior, case.k_new]).float()
+    v = torch.cat([case.v_prior, case.v_new]).float()
+    for h in range(3):
+        assert case.k_scale_h[h].item() == float(np.float32(k[:, h].abs().max().item()) / np.float32(448.0))
+        assert case.v_scale_h[h].item() == float(np.float32(v[:, h].abs().max().item()) / np.float32(448.0))
+    assert case.k_scale == float(case.k_scale_h.max()) and case.v_scale == float(case.v_scale_h.max())
+
+
 def load_norm_rope_rounding():
     """The exact-arithmetic row of tests/golden/norm_rope_rounding.txt."""
     vals = {}

@@ -51,6 +51,13 @@ def minmax_scale(*tensors) -> float:
     return float(np.float32(amax) / np.float32(E4M3_MAX))
 
 
+def minmax_scales_per_head(*tensors) -> torch.Tensor:
+    """Static symmetric per-head scales of [T][Hkv][D] tensors: fp32(max |x| over
+    head h) / 448 in fp32, one per KV head (float32 [Hkv], CPU)."""
+    amax = torch.stack([t.abs().float().amax(dim=(0, 2)) for t in tensors]).amax(dim=0).cpu()
+    return (amax.to(torch.float32) / torch.tensor(E4M3_MAX, dtype=torch.float32)).to(torch.float32)
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (for the oracle)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -106,6 +113,8 @@ class LayerCase:
     v_scale: float
     window_left: int                 # -1 = global
     sm_scale: float = 1.0 / math.sqrt(HEAD_DIM)
+    k_scale_h: Optional[torch.Tensor] = None   # fp32 [Hkv] per-head minmax/448 scales of the whole K
+    v_scale_h: Optional[torch.Tensor] = None
 
     @property
     def B(self):
@@ -150,7 +159,8 @@ def layer_case(seed: int, seq_lens: List[int], M: int, page_size: int, window: O
     return LayerCase(layout=layout, M=M, q=q, k_prior=k_all[pi], v_prior=v_all[pi],
                      slots_prior=torch.cat(slots_prior), k_new=k_all[ni], v_new=v_all[ni],
                      slots_new=torch.cat(slots_new), k_scale=k_scale, v_scale=v_scale,
-                     window_left=(window - 1) if window else -1)
+                     window_left=(window - 1) if window else -1,
+                     k_scale_h=minmax_scales_per_head(k_all), v_scale_h=minmax_scales_per_head(v_all))
 
 
 # ------------------------------------------------------- fused-norm inputs
