@@ -97,6 +97,23 @@ int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping
                        int cache_dtype, void* stream);
 
 /*
+ * fp8kv_cache_insert_per_head -- fp8kv_cache_insert on an E4M3 cache with one
+ * scale per KV head: head h of K (V) is encoded with k_scale[h] (v_scale[h]).
+ * An extension the pages do not use: their checkpoint asks for one static
+ * symmetric scale per tensor ("KV-cache precision decision", "What the
+ * official checkpoint requests", strategy "tensor"); a per-head scale keeps
+ * the same encoding with a finer calibration grain.
+ *
+ *   k_scale, v_scale (device) fp32 [Hkv], each > 0
+ *   every other argument, check and status as fp8kv_cache_insert with
+ *   cache_dtype = FP8KV_CACHE_E4M3.
+ */
+int fp8kv_cache_insert_per_head(const void* k, const void* v, const int64_t* slot_mapping, int T,
+                                int Hkv, int D, const float* k_scale, const float* v_scale,
+                                void* k_cache, void* v_cache, int num_pages, int page_size,
+                                void* stream);
+
+/*
  * fp8kv_qk_norm_rope_insert -- the Q/K RMSNorm + RoPE boundary fused with the
  * E4M3 insert ("calibrated FP8 KV on Intel B70", "Initial optimization order",
  * item 3; ledger table "Result progression", row "Exact fusion stack").
@@ -232,6 +249,33 @@ int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const voi
                                  const float* k_scale, const float* v_scale, float sm_scale,
                                  int window_left, int split_tokens, void* workspace,
                                  size_t workspace_bytes, void* out, void* stream);
+
+/*
+ * fp8kv_paged_attention_per_head, fp8kv_append_paged_attention_per_head --
+ * fp8kv_paged_attention and fp8kv_append_paged_attention on an E4M3 cache
+ * written with per-head scales (fp8kv_cache_insert_per_head): KV head hk is
+ * dequantized with k_scale[hk], v_scale[hk] (device fp32 [Hkv]), and the
+ * append encodes head hk's new tokens with them:
+ *     Kd = decode(k_code) * k_scale[hk],  Vd = decode(v_code) * v_scale[hk]
+ * Every other argument, kernel choice, check and status as the per-tensor
+ * entry points with cache_dtype = FP8KV_CACHE_E4M3 (the same workspace size).
+ */
+int fp8kv_paged_attention_per_head(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, int max_pages_per_seq,
+                                   const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq,
+                                   int Hkv, int D, int page_size, int num_pages, const float* k_scale,
+                                   const float* v_scale, float sm_scale, int window_left,
+                                   int split_tokens, void* workspace, size_t workspace_bytes, void* out,
+                                   void* stream);
+
+int fp8kv_append_paged_attention_per_head(const void* k_new, const void* v_new, const void* q,
+                                          void* k_cache, void* v_cache, const int32_t* block_table,
+                                          int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                          int B, int M, int Hq, int Hkv, int D, int page_size,
+                                          int num_pages, const float* k_scale, const float* v_scale,
+                                          float sm_scale, int window_left, int split_tokens,
+                                          void* workspace, size_t workspace_bytes, void* out,
+                                          void* stream);
 
 /*
  * fp8kv_paged_attention_layers -- the verifier step of several layers in one

@@ -132,6 +132,40 @@ def test_insert_validation(L):
     assert g(*bad) == 2
 
 
+def test_per_head_entries_validation_needs_no_device(L):
+    """The per-head entry points check their arguments on the host like the
+    per-tensor ones (E4M3 cache implied): missing scales, sizes, B/T = 0."""
+    f = L.fp8kv_cache_insert_per_head
+    args = [P16, P16, P16, 4, 8, 128, P16, P16, P16, P16, 16, 32, NULL]
+    assert f(*[NULL if i == 6 else a for i, a in enumerate(args)]) == 1      # k_scale missing
+    assert f(*[96 if i == 5 else a for i, a in enumerate(args)]) == 2        # D != 128
+    assert f(*[0 if i == 3 else a for i, a in enumerate(args)]) == 0         # T = 0
+    g = L.fp8kv_paged_attention_per_head
+    a = [P16, P16, P16, P16, 4, P16, 100, 1, 12, 72, 8, 128, 32, 16, P16, P16, 0.088, -1, 32, P16, 1 << 30, P16,
+         NULL]
+    assert g(*[NULL if i == 15 else x for i, x in enumerate(a)]) == 1        # v_scale missing
+    assert g(*[64 if i == 11 else x for i, x in enumerate(a)]) == 2          # D != 128
+    assert g(*[0 if i == 7 else x for i, x in enumerate(a)]) == 0            # B = 0
+    h = L.fp8kv_append_paged_attention_per_head
+    assert h(NULL, P16, *a) == 1                                               # k_new missing
+    assert h(NULL, NULL, *[0 if i == 7 else x for i, x in enumerate(a)]) == 0
+
+
+def test_per_head_binding_checks_scale_count():
+    if not torch.cuda.is_available():
+        k = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
+        with pytest.raises(ValueError):                 # CPU tensors are refused first
+            fp8kv.fp8kv_cache_insert_per_head(k, k, torch.zeros(1, dtype=torch.int64), torch.ones(8), torch.ones(8),
+                                              torch.zeros(1, 8, 32, 128, dtype=torch.uint8),
+                                              torch.zeros(1, 8, 32, 128, dtype=torch.uint8))
+        return
+    k = torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(1, 8, 32, 128, dtype=torch.uint8, device="cuda")
+    with pytest.raises(ValueError):
+        fp8kv.fp8kv_cache_insert_per_head(k, k, torch.zeros(1, dtype=torch.int64, device="cuda"),
+                                          torch.ones(7, device="cuda"), torch.ones(8, device="cuda"), c, c)
+
+
 def test_plan_and_workspace_host_logic(L):
     # explicit partitions: 131072 keys of page 64 in partitions of 2048 keys
     ns, st = fp8kv.fp8kv_paged_attention_plan(1, 1, 72, 8, 128, 64, 131072, -1, 2048)

@@ -277,7 +277,7 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
         }
         const float log2e = 1.4426950408889634f;
         if (FP8) {
-            const float ks = *P.k_scale;
+            const float ks = P.k_scale[P.scale_stride * hk];
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
                 float amax = 0.f;
@@ -530,7 +530,7 @@ __device__ __forceinline__ void attention_body(const CUtensorMap& tm_k, const CU
     asm volatile("bar.sync 1, %0;" ::"r"(n_cons * 32) : "memory");
     if (!ok) return;
 
-    const float vs = FP8 ? *P.v_scale : 1.0f;
+    const float vs = FP8 ? P.v_scale[P.scale_stride * hk] : 1.0f;
     const int tid = threadIdx.x;
     for (int item = tid; item < P.R * 32; item += n_cons * 32) {
         const int r = item >> 5, d4 = (item & 31) * 4;
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
                                                           int Hq, int G, int tile_rows, int mpps,
                                                           int page_size, int window_left, int split_pages,
                                                           int num_splits, int max_seq_len, const float* v_scale,
-                                                          uint16_t* out) {
+                                                          int scale_stride, uint16_t* out) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -620,7 +620,7 @@ __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restric
     float den = 0.f;
     if (F16) {
         const uint16_t* ph = (const uint16_t*)ws_o + row * num_splits * 128 + lane * 4;
-        const float vs = *v_scale;
+        const float vs = v_scale[scale_stride * ((int)(row % Hq) / G)];   // this row's KV head
         if (ns <= 16) {
             // every load in flight at once: (max, sum) of partition j on lane j
             // and this lane's four dims of every partition; then the arithmetic
@@ -977,9 +977,9 @@ static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 static int attention_call(const void* k_new, const void* v_new, const void* q, const void* k_cache,
                           const void* v_cache, int cache_dtype, const int32_t* block_table, int max_pages_per_seq,
                           const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq, int Hkv, int D,
-                          int page_size, int num_pages, const float* k_scale, const float* v_scale, float sm_scale,
-                          int window_left, int split_tokens, void* workspace, size_t workspace_bytes, void* out,
-                          void* stream) {
+                          int page_size, int num_pages, const float* k_scale, const float* v_scale, int scale_stride,
+                          float sm_scale, int window_left, int split_tokens, void* workspace, size_t workspace_bytes,
+                          void* out, void* stream) {
     if (cache_dtype != FP8KV_CACHE_E4M3 && cache_dtype != FP8KV_CACHE_BF16) return FP8KV_ERR_INVALID_ARG;
     const bool fp8 = cache_dtype == FP8KV_CACHE_E4M3;
     Plan plan;
@@ -1014,6 +1014,7 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     P.seq_lens = seq_lens;
     P.k_scale = k_scale;
     P.v_scale = v_scale;
+    P.scale_stride = scale_stride;
     const size_t rows = (size_t)B * M * Hq;
     P.ws_o = plan.num_splits > 1 ? (float*)workspace : nullptr;
     P.ws_ml = plan.num_splits > 1 ? P.ws_o + rows * plan.num_splits * 128 : nullptr;
@@ -1066,7 +1067,7 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
         P.num_pages = num_pages;
     } else if (k_new) {
         rc = launch_append(k_new, v_new, seq_lens, block_table, max_pages_per_seq, B, M, Hkv, k_scale, v_scale,
-                           (void*)k_cache, (void*)v_cache, num_pages, page_size, fp8, s);
+                           scale_stride, (void*)k_cache, (void*)v_cache, num_pages, page_size, fp8, s);
         if (rc) return rc;
     }
     if (use_tc)
@@ -1082,7 +1083,7 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
                                    dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, (const float*)P.ws_o,
                                    (const float*)P.ws_ml, seq_lens, B, M, Hq, P.G, use_tc ? 128 : P.R,
                                    max_pages_per_seq, page_size, window_left, plan.split_pages, plan.num_splits,
-                                   max_seq_len, k_scale ? v_scale : nullptr, (uint16_t*)out);
+                                   max_seq_len, k_scale ? v_scale : nullptr, scale_stride, (uint16_t*)out);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return FP8KV_ERR_CUDA;
@@ -1113,8 +1114,20 @@ extern "C" int fp8kv_paged_attention(const void* q, const void* k_cache, const v
                                      int window_left, int split_tokens, void* workspace, size_t workspace_bytes,
                                      void* out, void* stream) {
     return attention_call(nullptr, nullptr, q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq,
-                          seq_lens, max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, sm_scale,
-                          window_left, split_tokens, workspace, workspace_bytes, out, stream);
+                          seq_lens, max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, 0,
+                          sm_scale, window_left, split_tokens, workspace, workspace_bytes, out, stream);
+}
+
+extern "C" int fp8kv_paged_attention_per_head(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* block_table, int max_pages_per_seq,
+                                              const int32_t* seq_lens, int max_seq_len, int B, int M, int Hq,
+                                              int Hkv, int D, int page_size, int num_pages, const float* k_scale,
+                                              const float* v_scale, float sm_scale, int window_left,
+                                              int split_tokens, void* workspace, size_t workspace_bytes, void* out,
+                                              void* stream) {
+    return attention_call(nullptr, nullptr, q, k_cache, v_cache, FP8KV_CACHE_E4M3, block_table, max_pages_per_seq,
+                          seq_lens, max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, 1,
+                          sm_scale, window_left, split_tokens, workspace, workspace_bytes, out, stream);
 }
 
 extern "C" int fp8kv_append_paged_attention(const void* k_new, const void* v_new, const void* q, void* k_cache,
@@ -1126,8 +1139,22 @@ extern "C" int fp8kv_append_paged_attention(const void* k_new, const void* v_new
                                             size_t workspace_bytes, void* out, void* stream) {
     if (B > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
     return attention_call(k_new, v_new, q, k_cache, v_cache, cache_dtype, block_table, max_pages_per_seq, seq_lens,
-                          max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, sm_scale,
+                          max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, 0, sm_scale,
                           window_left, split_tokens, workspace, workspace_bytes, out, stream);
+}
+
+extern "C" int fp8kv_append_paged_attention_per_head(const void* k_new, const void* v_new, const void* q,
+                                                     void* k_cache, void* v_cache, const int32_t* block_table,
+                                                     int max_pages_per_seq, const int32_t* seq_lens, int max_seq_len,
+                                                     int B, int M, int Hq, int Hkv, int D, int page_size,
+                                                     int num_pages, const float* k_scale, const float* v_scale,
+                                                     float sm_scale, int window_left, int split_tokens,
+                                                     void* workspace, size_t workspace_bytes, void* out,
+                                                     void* stream) {
+    if (B > 0 && (!k_new || !v_new)) return FP8KV_ERR_INVALID_ARG;
+    return attention_call(k_new, v_new, q, k_cache, v_cache, FP8KV_CACHE_E4M3, block_table, max_pages_per_seq,
+                          seq_lens, max_seq_len, B, M, Hq, Hkv, D, page_size, num_pages, k_scale, v_scale, 1,
+                          sm_scale, window_left, split_tokens, workspace, workspace_bytes, out, stream);
 }
 
 // ================================================ allocation-free variant

@@ -10,8 +10,9 @@ struct AttnParams {
     const uint16_t* q;          // bf16 [B][M][Hq][128]
     const int32_t* block_table; // [B][mpps]
     const int32_t* seq_lens;    // [B]
-    const float* k_scale;
+    const float* k_scale;       // [1] per tensor, or [Hkv] per KV head (scale_stride 1)
     const float* v_scale;
+    int scale_stride;           // 0: one scale per tensor; 1: scale of KV head hk at [hk]
     float* ws_o;                // [B*M*Hq][num_splits][128]
     float* ws_ml;               // [B*M*Hq][num_splits][2]
     uint16_t* out;              // bf16 [B][M][Hq][128]
@@ -73,7 +74,8 @@ bool cache_map(CUtensorMap* m, const void* base, bool fp8, int Hkv, int PS, int 
 
 // Append kernel (insert.cu): the same encoding for the other attention paths.
 int launch_append(const void* k, const void* v, const int32_t* seq_lens, const int32_t* block_table, int mpps, int B,
-                  int M, int Hkv, const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
+                  int M, int Hkv, const float* k_scale, const float* v_scale, int scale_stride, void* k_cache,
+                  void* v_cache,
                   int num_pages, int page_size, bool fp8, cudaStream_t s);
 
 // Host launcher of the tcgen05 kernel (attention_tc.cu).  Returns

@@ -299,7 +299,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // bytes there cannot reach the output.
         const int ct = converter_index(warp) * 32 + lane;
         const int n_app = appends ? app_hi - app_lo : 0;
-        const float ksc = appends ? *P.k_scale : 1.f, vsc = appends ? *P.v_scale : 1.f;
+        const float ksc = appends ? P.k_scale[P.scale_stride * hk] : 1.f;
+        const float vsc = appends ? P.v_scale[P.scale_stride * hk] : 1.f;
         // the append item `it`: one 8-element chunk of K and of V of a new token
         auto app_item = [&](int it, uint2& kc, uint2& vc, int& pos, int& chunk) {
             pos = app_lo + (it >> 4);
@@ -419,7 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         const int p_r = L - P.M + m;
         const int lo_r = (P.window_left >= 0) ? max(0, p_r - P.window_left) : 0;
         const int64_t row_idx = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + rr % P.G;
-        const float vs = *P.v_scale;
+        const float vs = P.v_scale[P.scale_stride * hk];
         // rows past M*G get Q = 0: their (unused) weights stay finite and their
         // lanes take the same unmasked path as the real rows
         const bool pad = r >= RL;
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             }
             const int sh = max(-100, min(100, 7 - e));
             const float scale = ldexpf(1.0f, sh);
-            mult = (*P.k_scale) * P.sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
+            mult = P.k_scale[P.scale_stride * hk] * P.sm_scale * 1.4426950408889634f * ldexpf(1.0f, -sh);
             uint32_t hw[16], lw[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
@@ -663,7 +664,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         __syncwarp();
         cluster_sync_all();
         if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
-            const float vsc = *P.v_scale;
+            const float vsc = P.v_scale[P.scale_stride * hk];
             const int C = P.cluster, slots = (RL + C - 1) / C;
             for (int k = warp; k < slots && split + C * k < RL; k += WARPS) {
                 const int r = split + C * k;

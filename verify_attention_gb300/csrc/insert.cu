@@ -24,7 +24,7 @@ int status_insert(unsigned int* s, int clear) { return read_status(s, clear); }
 template <bool FP8>
 __global__ void __launch_bounds__(256) insert_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
-    int T, int Hkv, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+    int T, int Hkv, const float* __restrict__ k_scale, const float* __restrict__ v_scale, int scale_stride,
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, int64_t num_slots, int page_size) {
     pdl_launch_dependents();
     pdl_wait();
@@ -38,7 +38,8 @@ __global__ void __launch_bounds__(256) insert_kernel(
     // first use, one memory round trip instead of two
     const int64_t slot = slots[t];
     const uint4 kx = k[i], vx = v[i];
-    const float ks = FP8 ? *k_scale : 1.f, vs = FP8 ? *v_scale : 1.f;
+    // one scale per tensor (stride 0) or per KV head (stride 1)
+    const float ks = FP8 ? k_scale[scale_stride * h] : 1.f, vs = FP8 ? v_scale[scale_stride * h] : 1.f;
     if (slot < 0) return;
     if (slot >= num_slots) {
         if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
@@ -64,8 +65,8 @@ template <bool FP8>
 __global__ void __launch_bounds__(256) append_kernel(
     const uint4* __restrict__ k, const uint4* __restrict__ v, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ block_table, int mpps, int B, int M, int Hkv, const float* __restrict__ k_scale,
-    const float* __restrict__ v_scale, uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
-    int num_pages, int page_size) {
+    const float* __restrict__ v_scale, int scale_stride, uint8_t* __restrict__ k_cache,
+    uint8_t* __restrict__ v_cache, int num_pages, int page_size) {
     pdl_launch_dependents();
     pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(256) append_kernel(
     const int b = (int)(bm / M), m = (int)(bm % M);
     const int L = seq_lens[b];
     const uint4 kx = k[i], vx = v[i];
-    const float ks = FP8 ? *k_scale : 1.f, vs = FP8 ? *v_scale : 1.f;
+    const float ks = FP8 ? k_scale[scale_stride * h] : 1.f, vs = FP8 ? v_scale[scale_stride * h] : 1.f;
     const int pos = L - M + m;
     if (L < M || (L + page_size - 1) / page_size > mpps) {
         if (chunk == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
@@ -99,14 +100,14 @@ __global__ void __launch_bounds__(256) append_kernel(
 }
 
 int launch_append(const void* k, const void* v, const int32_t* seq_lens, const int32_t* block_table, int mpps, int B,
-                  int M, int Hkv, const float* k_scale, const float* v_scale, void* k_cache, void* v_cache,
-                  int num_pages, int page_size, bool fp8, cudaStream_t s) {
+                  int M, int Hkv, const float* k_scale, const float* v_scale, int scale_stride, void* k_cache,
+                  void* v_cache, int num_pages, int page_size, bool fp8, cudaStream_t s) {
     const int64_t items = (int64_t)B * M * Hkv * 16;
     const int64_t blocks = (items + 255) / 256;
     if (blocks > 0x7fffffff) return FP8KV_ERR_UNSUPPORTED;
     cudaError_t e = launch_pdl(fp8 ? append_kernel<true> : append_kernel<false>, dim3((unsigned)blocks), dim3(256), 0,
                                s, (const uint4*)k, (const uint4*)v, seq_lens, block_table, mpps, B, M, Hkv, k_scale,
-                               v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache, num_pages, page_size);
+                               v_scale, scale_stride, (uint8_t*)k_cache, (uint8_t*)v_cache, num_pages, page_size);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
@@ -251,10 +252,9 @@ extern "C" int fp8kv_selftest_bounded_wait(unsigned int limit_us, void* stream) 
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-extern "C" int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping, int T,
-                                  int Hkv, int D, const float* k_scale, const float* v_scale,
-                                  void* k_cache, void* v_cache, int num_pages, int page_size,
-                                  int cache_dtype, void* stream) {
+static int cache_insert(const void* k, const void* v, const int64_t* slot_mapping, int T, int Hkv, int D,
+                        const float* k_scale, const float* v_scale, int scale_stride, void* k_cache, void* v_cache,
+                        int num_pages, int page_size, int cache_dtype, void* stream) {
     if (T < 0 || Hkv <= 0 || num_pages <= 0) return FP8KV_ERR_INVALID_ARG;
     if (cache_dtype != FP8KV_CACHE_E4M3 && cache_dtype != FP8KV_CACHE_BF16) return FP8KV_ERR_INVALID_ARG;
     if (D != 128) return FP8KV_ERR_UNSUPPORTED;
@@ -272,9 +272,25 @@ extern "C" int fp8kv_cache_insert(const void* k, const void* v, const int64_t* s
     const int64_t num_slots = (int64_t)num_pages * page_size;
     cudaError_t e = launch_pdl(cache_dtype == FP8KV_CACHE_E4M3 ? insert_kernel<true> : insert_kernel<false>,
                                dim3((unsigned)blocks), dim3(threads), 0, s, (const uint4*)k, (const uint4*)v,
-                               slot_mapping, T, Hkv, k_scale, v_scale, (uint8_t*)k_cache, (uint8_t*)v_cache,
-                               num_slots, page_size);
+                               slot_mapping, T, Hkv, k_scale, v_scale, scale_stride, (uint8_t*)k_cache,
+                               (uint8_t*)v_cache, num_slots, page_size);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
+}
+
+extern "C" int fp8kv_cache_insert(const void* k, const void* v, const int64_t* slot_mapping, int T,
+                                  int Hkv, int D, const float* k_scale, const float* v_scale,
+                                  void* k_cache, void* v_cache, int num_pages, int page_size,
+                                  int cache_dtype, void* stream) {
+    return cache_insert(k, v, slot_mapping, T, Hkv, D, k_scale, v_scale, 0, k_cache, v_cache, num_pages, page_size,
+                        cache_dtype, stream);
+}
+
+extern "C" int fp8kv_cache_insert_per_head(const void* k, const void* v, const int64_t* slot_mapping, int T,
+                                           int Hkv, int D, const float* k_scale, const float* v_scale,
+                                           void* k_cache, void* v_cache, int num_pages, int page_size,
+                                           void* stream) {
+    return cache_insert(k, v, slot_mapping, T, Hkv, D, k_scale, v_scale, 1, k_cache, v_cache, num_pages, page_size,
+                        FP8KV_CACHE_E4M3, stream);
 }
 
 extern "C" int fp8kv_qk_norm_rope_insert(const void* q, const void* k, const void* v,

@@ -53,6 +53,13 @@ def lib() -> ctypes.CDLL:
                                             i32, i32, vp, vp, f32, i32, i32, vp, sz, vp, vp]
         L.fp8kv_append_paged_attention.restype = i32
         L.fp8kv_append_paged_attention.argtypes = [vp, vp] + L.fp8kv_paged_attention.argtypes
+        L.fp8kv_cache_insert_per_head.restype = i32
+        L.fp8kv_cache_insert_per_head.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, i32, i32, vp]
+        L.fp8kv_paged_attention_per_head.restype = i32
+        L.fp8kv_paged_attention_per_head.argtypes = [vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32,
+                                                     i32, i32, vp, vp, f32, i32, i32, vp, sz, vp, vp]
+        L.fp8kv_append_paged_attention_per_head.restype = i32
+        L.fp8kv_append_paged_attention_per_head.argtypes = [vp, vp] + L.fp8kv_paged_attention_per_head.argtypes
         L.fp8kv_paged_attention_noalloc.restype = i32
         L.fp8kv_paged_attention_noalloc.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
                                                     i32, i32, i32, vp, vp, f32, i32, i32, vp, vp]
@@ -126,6 +133,27 @@ def fp8kv_cache_insert(k, v, slot_mapping, k_scale, v_scale, k_cache, v_cache, s
                                   _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), num_pages, page_size,
                                   dt, _stream(stream))
     _check("fp8kv_cache_insert", rc)
+
+
+def _head_scales(k_scale, v_scale, Hkv):
+    for t, n in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        _dev(t, n, torch.float32)
+        if t.numel() != Hkv:
+            raise ValueError(f"{n} must hold one fp32 scale per KV head ({Hkv}), got {t.numel()}")
+
+
+def fp8kv_cache_insert_per_head(k, v, slot_mapping, k_scale, v_scale, k_cache, v_cache, stream=None):
+    """fp8kv_cache_insert on an E4M3 cache with per-head scales fp32 [Hkv]."""
+    _dev(k, "k", torch.bfloat16), _dev(v, "v", torch.bfloat16)
+    _dev(slot_mapping, "slot_mapping", torch.int64)
+    _dev(k_cache, "k_cache", torch.uint8), _dev(v_cache, "v_cache", torch.uint8)
+    T, Hkv, D = k.shape
+    _head_scales(k_scale, v_scale, Hkv)
+    num_pages, _, page_size, _ = k_cache.shape
+    rc = lib().fp8kv_cache_insert_per_head(_ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, _ptr(k_scale),
+                                           _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), num_pages, page_size,
+                                           _stream(stream))
+    _check("fp8kv_cache_insert_per_head", rc)
 
 
 def fp8kv_qk_norm_rope_insert(q, k, v, positions, q_norm_w, k_norm_w, eps, cos_sin, q_out,
@@ -221,6 +249,54 @@ def fp8kv_append_paged_attention(k_new, v_new, q, k_cache, v_cache, block_table,
         workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
     _check("fp8kv_append_paged_attention", rc)
     return out
+
+
+def fp8kv_paged_attention_per_head(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale,
+                                   sm_scale, window_left=-1, split_tokens=0, workspace=None, out=None,
+                                   num_pages=None, k_new=None, v_new=None, stream=None):
+    """fp8kv_paged_attention on an E4M3 cache with per-head scales fp32 [Hkv];
+    with k_new, v_new (bf16 [B][M][Hkv][D]) the append variant
+    (fp8kv_append_paged_attention_per_head)."""
+    _dev(q, "q", torch.bfloat16), _dev(k_cache, "k_cache", torch.uint8), _dev(v_cache, "v_cache", torch.uint8)
+    _dev(block_table, "block_table", torch.int32), _dev(seq_lens, "seq_lens", torch.int32)
+    B, M, Hq, D = q.shape
+    P, Hkv, page_size, _ = k_cache.shape
+    _head_scales(k_scale, v_scale, Hkv)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new go together")
+    if k_new is not None:
+        _dev(k_new, "k_new", torch.bfloat16), _dev(v_new, "v_new", torch.bfloat16)
+        if tuple(k_new.shape) != (B, M, Hkv, D) or tuple(v_new.shape) != (B, M, Hkv, D):
+            raise ValueError("k_new, v_new must be [B][M][Hkv][D]")
+    if num_pages is None:
+        num_pages = P
+    need = fp8kv_paged_attention_workspace_size(B, M, Hq, Hkv, D, page_size, max_seq_len, window_left,
+                                                split_tokens)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    args = (_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+            int(max_seq_len), B, M, Hq, Hkv, D, page_size, int(num_pages), _ptr(k_scale), _ptr(v_scale),
+            float(sm_scale), int(window_left), int(split_tokens), _ptr(workspace),
+            workspace.numel() if workspace is not None else 0, _ptr(out), _stream(stream))
+    if k_new is None:
+        _check("fp8kv_paged_attention_per_head", lib().fp8kv_paged_attention_per_head(*args))
+    else:
+        _check("fp8kv_append_paged_attention_per_head",
+               lib().fp8kv_append_paged_attention_per_head(_ptr(k_new), _ptr(v_new), *args))
+    return out
+
+
+def fp8kv_append_paged_attention_per_head(k_new, v_new, q, k_cache, v_cache, block_table, seq_lens, max_seq_len,
+                                          k_scale, v_scale, sm_scale, window_left=-1, split_tokens=0,
+                                          workspace=None, out=None, num_pages=None, stream=None):
+    """fp8kv_append_paged_attention on an E4M3 cache with per-head scales fp32 [Hkv]."""
+    if k_new is None or v_new is None:
+        raise ValueError("k_new and v_new are required")
+    return fp8kv_paged_attention_per_head(q, k_cache, v_cache, block_table, seq_lens, max_seq_len, k_scale, v_scale,
+                                          sm_scale, window_left, split_tokens, workspace, out, num_pages, k_new,
+                                          v_new, stream)
 
 
 class PreparedAttention:
