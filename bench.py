@@ -1024,12 +1024,15 @@ def main():
                                  "gbs": achieved,
                                  "peak_source": f"{peak_src} bf16_tflops (MEASURED_PEAKS.json)"})
     if args.workload == "verify48":
-        # the step's two attention-call kinds, each against HBM
+        # the step's two attention-call kinds, each against HBM, and the
+        # step's own append + attention calls of each kind
         line["attention_calls"] = {}
         for kind, wl in (("sliding_512", 511), ("global", -1)):
             ls = layers_of_kind(w, wl)
             secs, disp = time_attention_calls(ls, stream, w.ws)
             line["attention_calls"][kind] = call_record(ls[0], secs, disp, hbm_peak)
+            ssecs, _ = time_attention_calls(ls, stream, w.ws, step=True)
+            line["attention_calls"][kind]["append_call_us"] = ssecs * 1e6
     if args.workload == "verify48":
         line["one_launch"] = one_launch_step(w, stream, args.steps, args.warmup, step_s, hbm_peak)
     if rank == 0 and args.workload == "verify48" and not args.no_extra:
