@@ -250,8 +250,12 @@ def _free_context(cases):
 
 
 def workload_page_size(name, page_size_arg):
-    """The page size a workload runs at (the verify step takes --page-size)."""
-    return page_size_arg if name == "verify48" else (64 if name in ("decode128k", "prefill16k") else 32)
+    """The page size a workload runs at: --page-size for the verify step and
+    the long-context decode, else the workload's own (verify step 32, decode
+    and prefill 64, serving mix 32)."""
+    if name in ("verify48", "decode128k") and page_size_arg is not None:
+        return page_size_arg
+    return {"verify48": 32, "decode128k": 64, "prefill16k": 64}.get(name, 32)
 
 
 def workload_description(name, page_size, cache_dtype="e4m3"):
@@ -924,7 +928,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="verify48", choices=["verify48", "decode128k", "serving64",
                                                                   "prefill16k"])
-    ap.add_argument("--page-size", type=int, default=32, choices=[32, 64])
+    ap.add_argument("--page-size", type=int, default=None, choices=[32, 64])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
