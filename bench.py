@@ -719,8 +719,8 @@ def cpu_baseline(name, page_size, target_s=12.0):
 # ------------------------------------------------ the step in one launch
 
 def one_launch_step(w: Workload, stream, steps, warmup, per_layer_step_s, hbm_peak):
-    """The same verify step through fp8kv_paged_attention_layers: all 48
-    layers' append + attention in one persistent launch (layer order kept),
+    """The workload's step through fp8kv_paged_attention_layers: every
+    layer's append + attention in one persistent launch (layer order kept),
     one prepared call per cache copy, each captured in a CUDA graph; timed
     like the per-layer step (same steps, same rotation over cache copies)."""
     from verify_attention_gb300 import fp8kv
@@ -774,7 +774,8 @@ def side_measurements(dev, stream, hbm_peak, bf16_peak):
       decode128k       12 long-context decode layers, E4M3 and BF16 cache at
                        page 64, E4M3 at page 32;
       prefill16k       a prefill chunk on the tensor cores;
-      serving64        the batched serving mix, per layer kind;
+      serving64        the batched serving mix, per layer kind, and its layers'
+                       append + attention per layer and in one launch;
       cfg1, cfg2       the single-layer configurations (rotating cache copies)."""
     out = {}
     torch.cuda.empty_cache()
@@ -828,6 +829,19 @@ def side_measurements(dev, stream, hbm_peak, bf16_peak):
         ls = layers_of_kind(w, wl)
         secs, disp = time_attention_calls(ls, stream, w.ws, reps=8)
         srv[kind] = call_record(ls[0], secs, disp, hbm_peak)
+    # the 8 layers' append + attention (plain insert of the new tokens, no
+    # norm/RoPE) as per-layer calls and as one persistent launch
+    fused = [l.fused for c in w.copies for l in c]
+    for c in w.copies:
+        for l in c:
+            l.fused = None
+    s_app, _ = _step_time(w, stream, steps=5)
+    srv["append_step_ms"] = s_app * 1e3
+    srv["one_launch"] = one_launch_step(w, stream, 5, 2, s_app, hbm_peak)
+    it = iter(fused)
+    for c in w.copies:
+        for l in c:
+            l.fused = next(it)
     out["serving64"] = srv
     del w
     torch.cuda.empty_cache()

@@ -312,8 +312,9 @@ int fp8kv_append_paged_attention_per_head(const void* k_new, const void* v_new, 
  *              them zero.  Calls sharing a workspace must not overlap on the
  *              GPU.
  * Supported: E4M3 cache, D = 128, page_size 32 or 64, 16 < M*Hq/Hkv <= 128
- * (one 128-row tile of verifier rows per KV head), B*Hkv <= the number of
- * SMs; other shapes return FP8KV_ERR_UNSUPPORTED.  Per-layer arguments are
+ * (one 128-row tile of verifier rows per KV head), any B (with more work
+ * units than SMs, a CTA runs several units of a layer one after another);
+ * other shapes return FP8KV_ERR_UNSUPPORTED.  Per-layer arguments are
  * validated as in fp8kv_paged_attention before anything is launched.
  * Device checks as fp8kv_paged_attention; a wait that runs out (2 s) sets
  * FP8KV_DEV_WAIT_TIMEOUT and the launch still ends.

@@ -148,3 +148,28 @@ def test_layers_workspace_too_small_launches_nothing():
     assert e.value.status == 3
     torch.cuda.synchronize()
     assert torch.isnan(d["out"].float()).all()                     # untouched
+
+
+def test_layers_more_groups_than_sms():
+    """24 sequences x 8 KV heads = 192 (sequence, KV head) groups, more than
+    the 152 SMs: CTAs run several units per layer and combine after them.
+    Four layers (global and sliding), ragged lengths, against the oracle and
+    the per-layer calls."""
+    g = torch.Generator().manual_seed(10600)
+    lens = torch.randint(300, 3000, (24,), generator=g).tolist()
+    cases = [gen.layer_case(10600 + i, lens, 12, 32, window=w) for i, w in enumerate([None, 512, None, 64])]
+    check_layers(cases, [True] * 4, impl="numpy")
+
+
+@pytest.mark.parametrize("ps", [32, 64])
+def test_layers_serving_mix_shape(ps):
+    """The batched serving mix's shape: 64 sequences of 1024..8192 tokens
+    (2048 work units per layer over the CTAs), a global and a sliding-window
+    layer: every row of every sequence against the oracle, and the cache
+    bytes."""
+    g = torch.Generator().manual_seed(10700 + ps)
+    lens = torch.randint(1024, 8193, (64,), generator=g).tolist()
+    cases = [gen.layer_case(10700 + ps + i, lens, 12, ps, window=w) for i, w in enumerate([None, 512])]
+    layers = check_layers(cases, [True, True], impl="numpy", compare_per_layer=False)
+    assert fp8kv().fp8kv_last_dispatch().startswith("attention_layers")
+    del layers

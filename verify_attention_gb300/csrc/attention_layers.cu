@@ -10,8 +10,8 @@
 //
 // One CTA per SM for the whole step (a cooperative launch, so that every CTA
 // is resident and the waits below always end).  Each layer is cut into work
-// units (sequence, KV head, key partition of whole 128-key tiles), unit u of
-// a layer going to CTA u.  A unit runs the pipeline of the single-layer
+// units (sequence, KV head, key partition of whole 128-key tiles), units u,
+// u + grid, u + 2 grid, ... of a layer going to CTA u in that order.  A unit runs the pipeline of the single-layer
 // tensor-memory kernel (attention_tc.cu): a TMA producer warp, one MMA
 // thread, six V-widening warps, eight softmax warps, with the same Q split,
 // masks, online softmax and tile layout.  What differs:
@@ -27,7 +27,9 @@
 //   * partitions of a (sequence, KV head) combine through the workspace:
 //     each writes its normalised partial (f16, in E4M3 code units) and its
 //     (max, sum); once a counter shows every partition of the group written,
-//     each partition's CTA combines a share of the group's rows;
+//     each partition's CTA combines a share of the group's rows -- after all
+//     of its own units of the layer, so that no CTA waits for a group while
+//     holding back a unit another CTA waits for;
 //   * appended tokens are written to the cache and patched into the staged
 //     tile that holds them, as in the single-layer kernel.
 // Every wait is bounded (mbarriers and the global counters: 2 s, then
@@ -66,6 +68,11 @@ constexpr int WARPS = 16, THREADS = WARPS * 32;
 constexpr int CONV_WARPS = 6, CONV_THREADS = CONV_WARPS * 32;
 constexpr int SOFT_THREADS = 256;
 
+// Barriers of the patched tiles, used in turn: the converters can be at most
+// STAGES tiles ahead of the MMA thread, so with one more barrier than stages
+// a barrier cannot complete again before the MMA thread has waited on it.
+constexpr int N_PATCH = STAGES + 1;
+
 enum {
     B_STG_FULL = 0,
     B_STG_EMPTY = B_STG_FULL + STAGES,
@@ -79,11 +86,10 @@ enum {
     B_Q_READY = B_O_FREE + 1,
     B_MMA_IDLE = B_Q_READY + 1,
     B_PAIR = B_MMA_IDLE + 1,                     // one per TMEM lane quarter: the two softmax warps
-    // new tokens patched into a staged tile: one barrier for the first and one
-    // for the second of the (at most two) tiles of a unit that hold them, so
-    // that no waiter can fall a whole phase behind
+    // new tokens patched into a staged tile: the CTA's patched tiles take
+    // these barriers in turn (N_PATCH of them, above)
     B_PATCH = B_PAIR + 4,
-    B_DEP = B_PATCH + 2,                         // converters: the previous layer is complete
+    B_DEP = B_PATCH + N_PATCH,                   // converters: the previous layer is complete (all six warps)
     B_COUNT = B_DEP + 1
 };
 
@@ -207,9 +213,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         mbar_init(bar(B_O_FREE), 8);
         mbar_init(bar(B_Q_READY), 8);
         mbar_init(bar(B_MMA_IDLE), 1);
-        mbar_init(bar(B_PATCH), CONV_WARPS);
-        mbar_init(bar(B_PATCH + 1), CONV_WARPS);
-        mbar_init(bar(B_DEP), 1);
+        for (int k = 0; k < N_PATCH; ++k) mbar_init(bar(B_PATCH + k), CONV_WARPS);
+        mbar_init(bar(B_DEP), CONV_WARPS);                 // every converter warp, the poller last
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
         fence_barrier_init();
     }
@@ -233,13 +238,13 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         int tg = 0;                                         // this CTA's tile count
         for (int l = 0; l < P.n_layers && ok; ++l) {
             const LayerDesc& D = P.layer[l];
-            if (u >= units_of(P, D)) continue;
-            const Unit U = unit_of<PS>(P, D, u, false);
-            if (!U.run) continue;
-            if (lane == 0) {
+            if (lane == 0 && u < units_of(P, D)) {
                 prefetch_tensormap(&D.tm_k);
                 prefetch_tensormap(&D.tm_v);
             }
+          for (int uu = u; uu < units_of(P, D) && ok; uu += gridDim.x) {
+            const Unit U = unit_of<PS>(P, D, uu, false);
+            if (!U.run) continue;
             const int32_t* bt = D.block_table + (int64_t)U.b * D.mpps + U.page_begin;
             int next = (lane < U.n_pages) ? bt[lane] : 0;
             for (int base = 0; base < U.n_pages && ok; base += 32) {
@@ -267,6 +272,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     __syncwarp();
                 }
             }
+          }
         }
         if (lane == 0) {   // never leave with copies into this CTA's shared memory in flight
             for (int t = max(0, tg - STAGES); t < tg; ++t) mbar_wait(bar(B_STG_FULL + t % STAGES), (t / STAGES) & 1);
@@ -276,11 +282,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         if (lane == 0) {
             constexpr uint32_t ID_QK = idesc(128, NK, false);     // kind::f8f6f4, E4M3 x E4M3
             constexpr uint32_t ID_PV = idesc(128, 128, true);     // kind::f16, V MN-major
-            int tg = 0, qi = 0, pa[2] = {0, 0};                     // tiles, units, uses of each patch barrier
+            int tg = 0, qi = 0, pc = 0;                             // tiles, units, patched tiles
             for (int l = 0; l < P.n_layers && ok; ++l) {
-                const LayerDesc& D = P.layer[l];
-                if (u >= units_of(P, D)) continue;
-                const Unit U = unit_of<PS>(P, D, u, false);
+              const LayerDesc& D = P.layer[l];
+              for (int uu = u; uu < units_of(P, D) && ok; uu += gridDim.x) {
+                const Unit U = unit_of<PS>(P, D, uu, false);
                 if (!U.run) continue;
                 ok = mbar_wait(bar(B_Q_READY), qi & 1);
                 fence_after();
@@ -289,7 +295,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                         const int g = tg + t, s = g % STAGES, sb = g & 1;
                         ok = mbar_wait(bar(B_STG_FULL + s), (g / STAGES) & 1);
                         if (ok && t >= U.app_t0 && t <= U.app_t1)
-                            ok = mbar_wait(bar(B_PATCH + (t - U.app_t0)), pa[t - U.app_t0] & 1);
+                            ok = mbar_wait(bar(B_PATCH + (pc + t - U.app_t0) % N_PATCH),
+                                           ((pc + t - U.app_t0) / N_PATCH) & 1);
                         if (!ok) break;
                         fence_after();
                         const uint32_t kt = smem_u32(stg + s * STG_BYTES);
@@ -323,7 +330,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 }
                 tg += U.n_tiles;
                 ++qi;
-                for (int k = 0; k <= U.app_t1 - U.app_t0 && k < 2; ++k) ++pa[k];
+                pc += U.app_t1 >= U.app_t0 ? U.app_t1 - U.app_t0 + 1 : 0;
+              }
             }
             // nothing the tensor cores still run may outlive the TMEM allocation
             mma_commit(bar(B_MMA_IDLE));
@@ -333,11 +341,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
     } else if (is_converter(warp)) {
         // ---------------------------------------------------------- V widening
         const int ct = converter_index(warp) * 32 + lane;
-        int tg = 0, di = 0, pa[2] = {0, 0};                 // tiles, dependency waits, patch-barrier uses
+        int tg = 0, di = 0, pc = 0;                         // tiles, dependency waits, patched tiles
         for (int l = 0; l < P.n_layers && ok; ++l) {
-            const LayerDesc& D = P.layer[l];
-            if (u >= units_of(P, D)) continue;
-            const Unit U = unit_of<PS>(P, D, u, false);
+          const LayerDesc& D = P.layer[l];
+          for (int uu = u; uu < units_of(P, D) && ok; uu += gridDim.x) {
+            const Unit U = unit_of<PS>(P, D, uu, false);
             if (!U.run) continue;
             const int n_app = U.app_hi - U.app_lo;
             uint2 kc0 = make_uint2(0, 0), vc0 = make_uint2(0, 0);
@@ -364,11 +372,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     // this head's new tokens to the cache (the cache-insert
                     // encoding), keeping the first item's codes for the patch
                     if (l > 0) {
-                        // the first converter warp polls, then releases the others
-                        if (ct == 0) {
-                            wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
-                            mbar_arrive(bar(B_DEP));
-                        }
+                        // the first converter warp polls, then releases the
+                        // others; every warp arrives, so that none can run a
+                        // whole phase ahead to the next unit's wait
+                        if (ct == 0) wait_counter(&done[l - 1], (unsigned)units_of(P, P.layer[l - 1]));
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(B_DEP));
                         ok = mbar_wait(bar(B_DEP), di & 1);
                         ++di;
                         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -411,9 +420,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     }
                     fence_proxy_async();                    // for the tensor cores' read of K
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(B_PATCH + (t - U.app_t0)));
+                    const int pk = pc + t - U.app_t0;          // this CTA's patched tile number
+                    if (lane == 0) mbar_arrive(bar(B_PATCH + pk % N_PATCH));
                     // every converter warp's rows are in place before V is read
-                    ok = mbar_wait(bar(B_PATCH + (t - U.app_t0)), pa[t - U.app_t0] & 1);
+                    ok = mbar_wait(bar(B_PATCH + pk % N_PATCH), (pk / N_PATCH) & 1);
                     if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
                 }
                 const int zlo = max(0, min(NK, U.lo0 - k0));
@@ -463,7 +473,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 }
             }
             tg += U.n_tiles;
-            for (int k = 0; k <= U.app_t1 - U.app_t0 && k < 2; ++k) ++pa[k];
+            pc += U.app_t1 >= U.app_t0 ? U.app_t1 - U.app_t0 + 1 : 0;
+          }
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -477,9 +488,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
         int tg = 0, qi = 0, pp = 0;                         // tiles, units, pair-barrier phases
         for (int l = 0; l < P.n_layers && ok; ++l) {
             const LayerDesc& D = P.layer[l];
-            if (u >= units_of(P, D)) continue;
-            const Unit U = unit_of<PS>(P, D, u, threadIdx.x == 128);
-            const int g_idx = U.b * P.Hkv + U.hk;
+            const int nu = units_of(P, D);
+            if (u >= nu) continue;
             // the queries depend on the previous layer: wait until all of its
             // units have written their output
             if (l > 0) {
@@ -491,12 +501,18 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 ok = soft_all(w);
                 if (!ok) break;
             }
+            // this CTA's units of the layer: units u, u + grid, ...  Every unit
+            // is counted (its group's partial, or its share of the layer's
+            // output), also after a failed wait, so that no CTA waits in vain.
+            for (int uu = u; uu < nu; uu += gridDim.x) {
+            const Unit U = unit_of<PS>(P, D, uu, threadIdx.x == 128);
+            const int g_idx = U.b * P.Hkv + U.hk;
             const int rr = min(r, RL - 1);
             const int m = rr / P.G;
             const int p_r = U.L - P.M + m;
             const int lo_r = (D.window_left >= 0) ? max(0, p_r - D.window_left) : 0;
             const int64_t row_idx = ((int64_t)U.b * P.M + m) * P.Hq + U.hk * P.G + rr % P.G;
-            if (U.run) {
+            if (ok && U.run) {
                 float mult;
                 {
                     // Q row split (as in the single-layer kernel): q' = q * 2^sh
@@ -693,16 +709,27 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                 tg += U.n_tiles;
                 ++qi;
             }
-            // ------------------------------------------- combine partitions
             ok = soft_all(ok);
             const bool multi = U.seq_ok && U.nsplit_b > 1 && U.nsplit_b <= D.num_splits;
-            if (multi) {
-                if (st == 0) {
-                    __threadfence();
-                    red_release_add(&grp[(size_t)l * P.B * P.Hkv + g_idx], 1u);
-                }
-                bool w = true;
-                if (st == 0) w = wait_counter(&grp[(size_t)l * P.B * P.Hkv + g_idx], (unsigned)D.num_splits);
+            if (st == 0) {
+                // partial written (the group's counter), or this unit's rows of
+                // the output written directly (the layer's counter)
+                __threadfence();
+                red_release_add(multi ? &grp[(size_t)l * P.B * P.Hkv + g_idx] : &done[l], 1u);
+            }
+            }
+            // ------------------------------------------- combine partitions
+            // Only after all of this CTA's units of the layer: a CTA never
+            // waits for a group while a unit it has yet to run belongs to
+            // another CTA's awaited group.  Each partition's CTA combines a
+            // share of its group's rows.
+            for (int uu = u; uu < nu; uu += gridDim.x) {
+                const Unit U = unit_of<PS>(P, D, uu, false);
+                const int g_idx = U.b * P.Hkv + U.hk;
+                const bool multi = U.seq_ok && U.nsplit_b > 1 && U.nsplit_b <= D.num_splits;
+                if (!multi) continue;
+                bool w = ok;
+                if (st == 0 && ok) w = wait_counter(&grp[(size_t)l * P.B * P.Hkv + g_idx], (unsigned)D.num_splits);
                 ok = soft_all(w && ok);
                 if (ok) {
                     // rows split, split + num_splits, ... of the group: one warp per row
@@ -745,12 +772,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_layers_kernel(const __gr
                     }
                 }
                 ok = soft_all(ok);
-            }
-            // this unit's share of the layer's output is written (counted even
-            // after a failed wait, so that no other CTA waits for it in vain)
-            if (st == 0) {
-                __threadfence();
-                red_release_add(&done[l], 1u);
+                // this unit's share of the layer's output is written (counted
+                // even after a failed wait, so that no other CTA waits for it in vain)
+                if (st == 0) {
+                    __threadfence();
+                    red_release_add(&done[l], 1u);
+                }
             }
         }
     }
@@ -889,7 +916,6 @@ extern "C" int fp8kv_paged_attention_layers(const fp8kv_layer* layers, int n_lay
     if (!workspace || workspace_bytes < need || !al16(workspace)) return FP8KV_ERR_WORKSPACE;
     const int grid = layers_max_grid();
     if (grid <= 0) return FP8KV_ERR_CUDA;
-    if ((int64_t)B * Hkv > grid) return FP8KV_ERR_UNSUPPORTED;   // one unit per CTA and layer
 
     static thread_local LayersParams P;          // 25 KB: kept off the stack
     P.n_layers = n_layers;
@@ -905,7 +931,12 @@ extern "C" int fp8kv_paged_attention_layers(const fp8kv_layer* layers, int n_lay
     P.part_o = (uint16_t*)((uint8_t*)workspace + counters_bytes(n_layers, B, Hkv));
     P.part_ml = (float*)(P.part_o + rows * kLayersMaxSplits * 128);
     const int tile_pages = 128 / page_size;
-    const int units_per_group = std::min(kLayersMaxSplits, grid / (B * Hkv));
+    // partitions per (sequence, KV head): about two units per CTA and layer,
+    // and for many sequences at least a quarter of the longest one each
+    // (units past the grid run one after another on the CTAs)
+    const int64_t groups = (int64_t)B * Hkv;
+    const int spread = (int)std::min<int64_t>(kLayersMaxSplits, std::max<int64_t>(1, (2 * grid + groups - 1) / groups));
+    const int units_per_group = std::min(kLayersMaxSplits, groups > grid / 2 ? std::max(4, spread) : spread);
     int max_splits_used = 1;
     for (int l = 0; l < n_layers; ++l) {
         const fp8kv_layer& A = layers[l];
