@@ -164,6 +164,42 @@ def test_single_sequence_cluster_combine(L, window, split, msl, cluster):
     assert_close(out, ref, f"L={L} split={split}")
 
 
+@pytest.mark.parametrize("ps,window,split", [(32, None, 128), (64, None, 256), (32, 300, 128)])
+def test_longest_first_partition_order(ps, window, split):
+    """Several sequences of verifier rows in several partitions: the CTAs take
+    the (sequence, partition) slots longest first from an order computed on
+    the device.  48 sequences of ragged lengths (some shorter than one tile,
+    so most of their slots are empty; more than 512 slots at 128-key
+    partitions), every row against the oracle."""
+    lens = np.random.default_rng(9400 + ps).integers(12, 1500, 48).tolist()
+    lens[5], lens[17] = 1500, 12
+    case = gen.layer_case(9400 + ps + split, lens, 12, ps, window=window)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    out = gpu_attention(case, kc, vc, ks, vs, split_tokens=split)
+    torch.cuda.synchronize()
+    d = fp8kv().fp8kv_last_dispatch()
+    assert d.startswith("attention_tc") and "order=longest_first" in d and "reduce=1" in d, d
+    assert_close(out, oracle_attention(case, okc, ovc), f"longest first ps={ps} split={split}")
+
+
+def test_longest_first_order_flags_a_bad_length():
+    """A sequence length below M in a longest-first call is flagged (by the
+    order kernel) and its slots get no CTA; the other sequences are exact."""
+    f = fp8kv()
+    case = gen.layer_case(9450, [700, 300, 1200], 12, 32)
+    kc, vc, ks, vs = gpu_caches(case)
+    okc, ovc = oracle_caches(case)
+    ref = oracle_attention(case, okc, ovc)
+    case.layout.seq_lens[1] = 5
+    f.fp8kv_device_status(clear=True)
+    out = gpu_attention(case, kc, vc, ks, vs, split_tokens=256, max_seq_len=1200)
+    torch.cuda.synchronize()
+    assert "order=longest_first" in f.fp8kv_last_dispatch()
+    assert f.fp8kv_device_status(clear=True) & f.DEV_BAD_SEQ_LEN
+    assert_close(out[[0, 2]], ref[[0, 2]], "other sequences")
+
+
 @pytest.mark.parametrize("M,G", [(2, 9), (2, 16), (6, 9), (8, 16), (12, 10), (16, 8), (3, 11)])
 def test_tensor_memory_kernel_row_counts(M, G):
     """Row counts 18..128 through the tcgen05 kernel, both page sizes."""

@@ -590,6 +590,70 @@ __global__ void __maxnreg__(kDecodeRegs) paged_decode_kernel(
 //     O = sum_p 2^(m_p - m*) O_p / sum_p 2^(m_p - m*) l_p;
 // those of the tensor-memory kernel (F16 = true) are f16 O_p / l_p in E4M3
 // code units: O = v_scale * sum_p w_p O_p / sum_p w_p, w_p = 2^(m_p - m*) l_p.
+// Longest-first order of the (sequence, partition) slots of a tcgen05 call
+// with one row tile of R rows (q = b * num_splits + s): slots ranked by
+// their number of 128-key tiles (in 63 classes of tiles_per_split), longest
+// first, written to order[0 .. n) (n = slots that hold keys) and -1 after
+// them.  One CTA.  Invalid sequence lengths hold no keys and are flagged as
+// the attention kernel flags them.
+__global__ void __launch_bounds__(512) lpt_order_kernel(const int32_t* __restrict__ seq_lens, int B, int M,
+                                                        int R, int G, int mpps, int page_size, int window_left,
+                                                        int split_pages, int num_splits, int max_seq_len,
+                                                        int32_t* __restrict__ order) {
+    __shared__ int count[64], start[64];
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, lane = tid & 31;
+    if (tid < 64) count[tid] = 0;
+    __syncthreads();
+    pdl_wait();
+    const int nslot = B * num_splits;
+    const int tiles_per_split = split_pages * page_size / 128;
+    auto cls = [&](int q) {
+        const int b = q / num_splits, s = q % num_splits;
+        const int L = seq_lens[b];
+        if (L < M || L > max_seq_len || (L + page_size - 1) / page_size > mpps) {
+            if (s == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+            return 0;
+        }
+        const int lo0 = (window_left >= 0) ? max(0, L - M - window_left) : 0;
+        const int first_page = lo0 / page_size, last_page = (L - M + (R - 1) / G) / page_size;
+        const int ns = (last_page - first_page + split_pages) / split_pages;
+        if (ns > num_splits) {
+            if (s == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+            return 0;
+        }
+        if (s >= ns) return 0;
+        const int n_pages = min(split_pages, last_page + 1 - (first_page + s * split_pages));
+        const int tiles = (n_pages * page_size + 127) / 128;
+        return 1 + (tiles - 1) * 63 / tiles_per_split;
+    };
+    for (int q = tid; q < nslot; q += blockDim.x) {
+        const int c = cls(q);
+        if (c) atomicAdd(&count[c], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+        // lane l: classes 63 - 2l and 62 - 2l, in that (descending) order
+        const int c0 = 63 - 2 * lane, c1 = 62 - 2 * lane;
+        const int n0 = count[c0], n1 = c1 > 0 ? count[c1] : 0;
+        int incl = n0 + n1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += x;
+        }
+        start[c0] = incl - n0 - n1;
+        if (c1 > 0) start[c1] = incl - n1;
+        if (lane == 31) start[0] = incl;                 // slots with keys
+    }
+    __syncthreads();
+    for (int j = start[0] + tid; j < nslot; j += blockDim.x) order[j] = -1;
+    for (int q = tid; q < nslot; q += blockDim.x) {
+        const int c = cls(q);
+        if (c) order[atomicAdd(&start[c], 1)] = q;
+    }
+}
+
 template <bool F16>
 __global__ void __launch_bounds__(256) attn_reduce_kernel(const float* __restrict__ ws_o,
                                                           const float* __restrict__ ws_ml,
@@ -913,7 +977,9 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
 }
 
 // Workspace: [partial O][partial (m, l)] when a sequence spans several
-// partitions (reserved even when the partitions combine on chip).
+// partitions (reserved even when the partitions combine on chip).  The
+// tcgen05 path writes f16 partial O in the first half of its area and keeps
+// its longest-first slot order (B * num_splits ints) in the second half.
 static size_t ws_bytes(int B, int M, int Hq, int Hkv, const Plan& p) {
     (void)Hkv;
     if (p.num_splits <= 1) return 0;
@@ -1059,6 +1125,11 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     // of a KV head run as one thread-block cluster and combine in distributed
     // shared memory
     P.cluster = (use_tc && B == 1 && RT == 1 && plan.num_splits > 1 && plan.num_splits <= 8) ? plan.num_splits : 0;
+    // several sequences split into partitions of unequal length: longest first
+    const bool lpt = use_tc && B > 1 && RT == 1 && plan.num_splits > 1;
+    if (lpt)
+        P.lpt_order = (const int32_t*)((const uint8_t*)workspace +
+                                       (size_t)B * M * Hq * plan.num_splits * 128 * sizeof(uint16_t));
     if (k_new && use_tc && RT == 1) {                               // appended in the kernel
         P.k_new = (const uint16_t*)k_new;
         P.v_new = (const uint16_t*)v_new;
@@ -1069,6 +1140,15 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
         rc = launch_append(k_new, v_new, seq_lens, block_table, max_pages_per_seq, B, M, Hkv, k_scale, v_scale,
                            scale_stride, (void*)k_cache, (void*)v_cache, num_pages, page_size, fp8, s);
         if (rc) return rc;
+    }
+    if (lpt) {
+        const cudaError_t e =
+            launch_pdl(lpt_order_kernel, dim3(1), dim3(512), 0, s, seq_lens, B, M, P.R, P.G, max_pages_per_seq,
+                       page_size, window_left, plan.split_pages, plan.num_splits, max_seq_len, (int32_t*)P.lpt_order);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return FP8KV_ERR_CUDA;
+        }
     }
     if (use_tc)
         rc = launch_attention_tc(tk, tv, P, s);
@@ -1093,9 +1173,10 @@ static int attention_call(const void* k_new, const void* v_new, const void* q, c
     if (use_tc)
         snprintf(buf, sizeof buf,
                  "attention_tc<ps=%d,e4m3> rows=%d row_tiles=%d tile=128x128 splits=%d split_tokens=%d "
-                 "grid=%dx%dx%d threads=%d cluster=%d reduce=%d",
+                 "grid=%dx%dx%d threads=%d cluster=%d reduce=%d order=%s",
                  page_size, P.R, RT, plan.num_splits, plan.split_tokens, plan.num_splits, Hkv * RT, B, tc_threads(),
-                 P.cluster > 1 ? P.cluster : 1, (plan.num_splits > 1 && P.cluster <= 1) ? 1 : 0);
+                 P.cluster > 1 ? P.cluster : 1, (plan.num_splits > 1 && P.cluster <= 1) ? 1 : 0,
+                 lpt ? "longest_first" : "grid");
     else
         snprintf(buf, sizeof buf,
                  "%s<ps=%d,%s> rows=%d row_tiles=%d key_groups=%d stages_per_group=%d splits=%d "

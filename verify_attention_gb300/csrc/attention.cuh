@@ -24,6 +24,12 @@ struct AttnParams {
     // partial results through distributed shared memory, without workspace
     // partials or the reduce kernel
     int cluster;
+    // tcgen05 path, several sequences in several partitions, one row tile:
+    // the (sequence, partition) slots q = b * num_splits + s longest first
+    // (lpt_order_kernel; -1 past the last slot that holds keys); CTA i (in
+    // launch order) takes slot lpt_order[i / Hkv] and KV head i % Hkv, so
+    // that the last CTAs to start are the shortest.  Null: grid order.
+    const int32_t* lpt_order;
     // append (tcgen05 path): the M new tokens of each sequence, bf16
     // [B][M][Hkv][128], are encoded into the cache at positions L - M + m by
     // the CTA whose partition holds them before it loads those pages; null

@@ -89,7 +89,6 @@ enum {
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
 __device__ __forceinline__ int converter_index(int warp) { return warp < 4 ? warp - 2 : warp - 10; }
 
-
 template <int PS>
 __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
@@ -108,7 +107,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     // blockIdx.y = row tile + RT * KV head: the row tiles of one head are
     // neighbours in launch order and share its pages in L2
     const int RT = (P.R + 127) >> 7;
-    const int split = blockIdx.x, rt = blockIdx.y % RT, hk = blockIdx.y / RT, b = blockIdx.z;
+    const int rt = blockIdx.y % RT;
+    int split = blockIdx.x, hk = blockIdx.y / RT, b = blockIdx.z;   // (longest-first: set after the wait)
     const int R0 = rt * 128, RL = min(128, P.R - R0);      // this CTA's rows R0 .. R0 + RL - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
-    if (warp == 1 && lane == 0) {
+    if (warp == 1 && lane == 0 && !P.lpt_order) {
         // L2 prefetch of the block-table entries this partition will read,
         // located from a read of the sequence length made before the wait for
         // the previous kernel: a hint only (the length and the entries used
@@ -172,10 +172,23 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     }
 
     pdl_wait();
+    bool have_work = true;
+    if (P.lpt_order) {
+        // CTA i: KV head i mod Hkv of the slot of rank i / Hkv, longest first
+        const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        const int q = P.lpt_order[lin / P.Hkv];
+        hk = lin % P.Hkv;
+        if (q < 0) {
+            have_work = false;
+        } else {
+            b = q / P.num_splits;
+            split = q % P.num_splits;
+        }
+    }
     const int L = P.seq_lens[b];
     const bool seq_ok = !(L < P.M || L > P.max_seq_len || (L + PS - 1) / PS > P.mpps);
-    bool run = seq_ok;                                      // uniform over the CTA
-    if (!seq_ok && threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
+    bool run = seq_ok && have_work;                         // uniform over the CTA
+    if (!seq_ok && !P.lpt_order && threadIdx.x == 0 && split == 0 && blockIdx.y == 0) flag(FP8KV_DEV_BAD_SEQ_LEN);
     // keys visible to any row of the tile: from the first row's window start
     // to the last row's position (row r is query m = r / G at L - M + m)
     const int hi0 = L - P.M + (R0 + RL - 1) / P.G;
@@ -580,6 +593,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const bool direct = nsplit_b == 1;
             const bool combine = !direct && P.cluster > 1;  // partial stays in shared memory
+            // the partition index, read again here rather than held through
+            // the tile loop
+            const int split_e =
+                P.lpt_order ? P.lpt_order[(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z)) / P.Hkv] %
+                                  P.num_splits
+                            : (int)blockIdx.x;
             // direct: bf16 of O * v_scale / l; partial (cluster or workspace):
             // f16 of O / l in code units (|x| <= 448, 11-bit mantissa) beside
             // its (max, sum), half the bytes of an fp32 partial
@@ -619,7 +638,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                         if (r < RL) {
                             const int C = P.cluster, slots = (RL + C - 1) / C;
                             const uint32_t a =
-                                dsmem_addr(recv + (split * slots + r / C) * 256 + half * 128 + c * 2, r % C);
+                                dsmem_addr(recv + (split_e * slots + r / C) * 256 + half * 128 + c * 2, r % C);
 #pragma unroll
                             for (int v4 = 0; v4 < 4; ++v4) st_dsmem_u32x4(a + 16 * v4, w[v4]);
                         }
@@ -635,7 +654,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 if (direct)
                     bulk_store(P.out + row_idx * 128 + 64 * half, smem_u32(row_stage), 128);
                 else
-                    bulk_store((uint16_t*)P.ws_o + (row_idx * P.num_splits + split) * 128 + 64 * half,
+                    bulk_store((uint16_t*)P.ws_o + (row_idx * P.num_splits + split_e) * 128 + 64 * half,
                                smem_u32(row_stage), 128);
                 bulk_commit();
                 bulk_wait_read();
@@ -643,10 +662,10 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             if (r < RL && !direct && half == 0) {
                 if (combine) {
                     const int C = P.cluster, slots = (RL + C - 1) / C;
-                    st_dsmem_f32x2(dsmem_addr(recv_ml + (split * slots + r / C) * 2, r % C), m_run, l_tot);
+                    st_dsmem_f32x2(dsmem_addr(recv_ml + (split_e * slots + r / C) * 2, r % C), m_run, l_tot);
                 } else {
-                    P.ws_ml[(row_idx * P.num_splits + split) * 2] = m_run;
-                    P.ws_ml[(row_idx * P.num_splits + split) * 2 + 1] = l_tot;
+                    P.ws_ml[(row_idx * P.num_splits + split_e) * 2] = m_run;
+                    P.ws_ml[(row_idx * P.num_splits + split_e) * 2 + 1] = l_tot;
                 }
             }
         }
@@ -740,6 +759,8 @@ int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Attn
     cudaError_t e;
     dim3 grid(P.num_splits, P.Hkv * RT, P.B);
     if (P.cluster > 1 && (P.cluster > 8 || P.cluster != P.num_splits)) return FP8KV_ERR_UNSUPPORTED;
+    if (P.lpt_order && (RT > 1 || P.cluster > 1 || (int64_t)P.B * P.num_splits * P.Hkv > INT32_MAX))
+        return FP8KV_ERR_UNSUPPORTED;
     e = launch_pdl_cluster(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
                            dim3(tc::THREADS), tc::SMEM, s, P.cluster, tk, tv, P);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
