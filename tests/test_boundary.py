@@ -196,8 +196,9 @@ def test_automatic_plans(L):
     """The automatic partition policy on a 152-SM GB300 (the planning default
     without a device): one wave of partitions for one long sequence of
     verifier rows, one tile per partition (a cluster) when it spans at most
-    8 tiles, one CTA per SM for decode, quarters of the longest sequence for a
-    large batch."""
+    8 tiles, one CTA per SM for decode, for a large batch halves of the
+    longest sequence (verifier rows, taken longest first) or quarters
+    (decode)."""
     import torch
     if torch.cuda.is_available():
         pytest.skip("plans depend on the device's SM count")
@@ -205,7 +206,8 @@ def test_automatic_plans(L):
     assert plan(1, 12, 72, 8, 128, 32, 8192, -1, 0) == (16, 512)     # 19 partitions max per head, whole tiles
     assert plan(1, 12, 72, 8, 128, 32, 8192, 511, 0) == (5, 128)     # window: 5 tiles -> 5-CTA cluster
     assert plan(1, 1, 72, 8, 128, 64, 131072, -1, 0) == (19, 6912)   # decode: 19 x 8 = 152 CTAs
-    assert plan(64, 12, 72, 8, 128, 32, 32768, -1, 0) == (4, 8192)   # batch: a quarter of 32768
+    assert plan(64, 12, 72, 8, 128, 32, 32768, -1, 0) == (2, 16384)  # verifier batch: halves, longest first
+    assert plan(64, 1, 72, 8, 128, 32, 32768, -1, 0) == (4, 8192)    # decode batch: quarters
 
 
 def test_plan_invariants_over_many_shapes(L):

@@ -942,12 +942,14 @@ static int make_plan(int B, int M, int Hq, int Hkv, int D, int PS, int max_seq_l
         const int64_t target = (M * (Hq / Hkv) <= 16 || RT > 1 ? 1LL : 2LL) * num_sms();
         const int per = (int)std::max<int64_t>(1, (target + units - 1) / units);
         sp = max(ceil_div(pages, per), 1024 / PS);
-        // with many units and long sequences, at least four partitions per
-        // sequence keep the longest ones from holding an SM alone at the end
-        // of the launch (sequence lengths are only known on the device)
-        // (prefill row tiles are many units already, and every partition
-        // writes a partial per row)
-        if (RT == 1 && ceil_div(pages, 4) >= 1024 / PS) sp = min(sp, ceil_div(pages, 4));
+        // with many units and long sequences, several partitions per sequence
+        // keep the longest ones from holding an SM alone at the end of the
+        // launch (sequence lengths are only known on the device): four on
+        // the decode kernel, two where the verifier rows of several sequences
+        // take their partitions longest first (prefill row tiles are many
+        // units already, and every partition writes a partial per row)
+        const int min_parts = (tc_rows(M, Hq, Hkv) && B > 1) ? 2 : 4;
+        if (RT == 1 && ceil_div(pages, min_parts) >= 1024 / PS) sp = min(sp, ceil_div(pages, min_parts));
         // one sequence of verifier rows (one CTA per SM): at most 8 tiles of
         // 128 keys get a tile per partition (the partitions of a KV head then
         // run as one thread-block cluster and combine on chip); longer ones
