@@ -21,8 +21,14 @@
 // One CTA per (partition, row tile x KV head, sequence), 16 warps:
 //   warp 0          TMA producer (128-key tiles: K and V E4M3, 2 or 4 pages);
 //                   allocates and frees the tensor memory
-//   warp 1          MMA issuer (one thread); completion via tcgen05.commit
-//   warps 2,3,12-15 V converters (192 threads)
+//   warp 1          MMA issuer (one thread); completion via tcgen05.commit.
+//                   Calls without tokens appended in the kernel issue P.V from
+//                   a second thread (warp 15), each thread waiting only for
+//                   its own operands: the tile loop is bound by the MMA issue
+//                   chain, which one thread serialises with its waits
+//   warps 2,3,12-15 V converters (192 threads; 160 when warp 15 issues P.V);
+//                   with appended tokens they also encode those, one item
+//                   per thread
 //   warps 4-11      softmax: warps 4+q and 8+q share TMEM lane quarter q (32
 //                   query rows, one per thread) and split the tile's 128 key
 //                   columns in halves; the row maximum of a tile is exchanged
@@ -65,7 +71,10 @@ constexpr int EPI_STRIDE = 272;
 static_assert(2 * 128 * EPI_STRIDE <= STAGES * STG_BYTES, "epilogue staging exceeds the stage ring");
 constexpr uint32_t TM_QH = 0, TM_QL = 32, TM_S = 64, TM_O = 320, TM_COLS = 512;
 constexpr int WARPS = 16, THREADS = WARPS * 32;
-constexpr int CONV_WARPS = 6, CONV_THREADS = CONV_WARPS * 32;
+// V converters: six warps (2, 3, 12-15), or five (2, 3, 12-14) when warp 15
+// issues P.V (DUAL: calls without appended tokens, whose converters also
+// encode the new tokens at the start of the launch)
+template <bool DUAL> __host__ __device__ constexpr int conv_warps() { return DUAL ? 5 : 6; }
 
 enum {
     B_STG_FULL = 0,
@@ -83,13 +92,18 @@ enum {
     // the (at most two) tiles that hold them, so that no waiter can fall a
     // whole phase behind
     B_PATCH = B_PAIR + 4,
-    B_COUNT = B_PATCH + 2
+    B_S_EMPTY = B_PATCH + 2,                    // per S buffer: P.V of the P over it done (DUAL)
+    B_COUNT = B_S_EMPTY + 2
 };
 
-__device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || warp >= 12; }
+template <bool DUAL>
+__device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || (warp >= 12 && warp < 12 + conv_warps<DUAL>() - 2); }
 __device__ __forceinline__ int converter_index(int warp) { return warp < 4 ? warp - 2 : warp - 10; }
 
-template <int PS>
+// DUAL: Q.K^T (warp 1) and P.V (warp 15) are issued by two threads, each
+// waiting only for its own operands; otherwise one thread issues Q.K^T(t)
+// then P.V(t - 1).
+template <int PS, bool DUAL>
 __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  AttnParams P) {
@@ -103,6 +117,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     uint64_t* bars = (uint64_t*)(recv + RECV_BYTES);
     uint32_t* tmem_slot = (uint32_t*)(bars + B_COUNT);
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    constexpr int CONV_WARPS = conv_warps<DUAL>(), CONV_THREADS = CONV_WARPS * 32;
 
     // blockIdx.y = row tile + RT * KV head: the row tiles of one head are
     // neighbours in launch order and share its pages in L2
@@ -131,7 +146,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         mbar_init(bar(B_O_DONE), 1);
         mbar_init(bar(B_O_FINAL), 1);
         mbar_init(bar(B_Q_READY), 8);
-        mbar_init(bar(B_MMA_IDLE), 1);
+        mbar_init(bar(B_MMA_IDLE), DUAL ? 2 : 1);               // the issuing threads
+        mbar_init(bar(B_S_EMPTY), 1);
+        mbar_init(bar(B_S_EMPTY + 1), 1);
         mbar_init(bar(B_PATCH), CONV_WARPS);
         mbar_init(bar(B_PATCH + 1), CONV_WARPS);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
@@ -258,53 +275,71 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             for (int t = max(0, issued_tiles - STAGES); t < issued_tiles; ++t)
                 mbar_wait(bar(B_STG_FULL + t % STAGES), (t / STAGES) & 1);
         }
-    } else if (warp == 1) {
-        // --------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t ID_QK = idesc(128, NK, false);     // kind::f8f6f4, E4M3 x E4M3
-            constexpr uint32_t ID_PV = idesc(128, 128, true);     // kind::f16, V MN-major
-            ok = mbar_wait(bar(B_Q_READY), 0);
+    } else if (warp == 1 || (DUAL && warp == 15)) {
+        // ------------------------------------------------------ MMA issue
+        constexpr uint32_t ID_QK = idesc(128, NK, false);         // kind::f8f6f4, E4M3 x E4M3
+        constexpr uint32_t ID_PV = idesc(128, 128, true);         // kind::f16, V MN-major
+        // S(t) = q'.K(t) into buffer t & 1
+        auto qk = [&](int t) -> bool {
+            const int s = t % STAGES, sb = t & 1;
+            if (!mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1)) return false;
+            // DUAL: the buffer holds P(t - 2) until its P.V has read it (one
+            // issuing thread orders that by issue order)
+            if (DUAL && t >= 2 && !mbar_wait(bar(B_S_EMPTY + sb), ((t >> 1) - 1) & 1)) return false;
+            if (t >= app_t0 && t <= app_t1 && !mbar_wait(bar(B_PATCH + (t - app_t0)), 0)) return false;
             fence_after();
-            for (int t = 0; t <= n_tiles && ok; ++t) {
-                if (t < n_tiles) {
-                    const int s = t % STAGES, sb = t & 1;
-                    ok = mbar_wait(bar(B_STG_FULL + s), (t / STAGES) & 1);
-                    if (ok && t >= app_t0 && t <= app_t1) ok = mbar_wait(bar(B_PATCH + (t - app_t0)), 0);
-                    if (!ok) break;
-                    fence_after();
-                    const uint32_t kt = smem_u32(stg + s * STG_BYTES);
+            const uint32_t kt = smem_u32(stg + s * STG_BYTES);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = sdesc(kt + ks * 32, 16, 1024);
-                        mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QH + 8 * ks, bd, ID_QK, ks > 0);
-                        mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QL + 8 * ks, bd, ID_QK, 1);
-                    }
-                    mma_commit(bar(B_S_FULL + sb));
-                    mma_commit(bar(B_STG_EMPTY + s));        // K of this stage read
-                }
-                if (t >= 1) {
-                    const int u = t - 1, ub = u & 1, vb = u % VBUFS;
-                    ok = mbar_wait(bar(B_P_FULL + ub), (u >> 1) & 1);
-                    if (ok) ok = mbar_wait(bar(B_V_FULL + vb), (u / VBUFS) & 1);
-                    if (!ok) break;
-                    fence_after();
-                    const uint32_t vf = smem_u32(vbuf + vb * VBUF_BYTES);
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t bd = sdesc(kt + ks * 32, 16, 1024);
+                mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QH + 8 * ks, bd, ID_QK, ks > 0);
+                mma_f8_ts(tmem + TM_S + sb * 128, tmem + TM_QL + 8 * ks, bd, ID_QK, 1);
+            }
+            mma_commit(bar(B_S_FULL + sb));
+            mma_commit(bar(B_STG_EMPTY + s));                // K of this stage read
+            return true;
+        };
+        // O += P(u).V(u)
+        auto pv = [&](int u) -> bool {
+            const int ub = u & 1, vb = u % VBUFS;
+            if (!mbar_wait(bar(B_P_FULL + ub), (u >> 1) & 1)) return false;
+            if (!mbar_wait(bar(B_V_FULL + vb), (u / VBUFS) & 1)) return false;
+            fence_after();
+            const uint32_t vf = smem_u32(vbuf + vb * VBUF_BYTES);
 #pragma unroll
-                    for (int kk = 0; kk < NK / 16; ++kk) {
-                        const uint64_t bd = sdesc(vf + kk * 2048, NK * 128, 1024);
-                        mma_f16_ts(tmem + TM_O, tmem + TM_S + ub * 128 + 8 * kk, bd, ID_PV, (u > 0 || kk > 0));
-                    }
-                    mma_commit(bar(B_O_DONE));
-                    mma_commit(bar(B_V_EMPTY + vb));
-                    if (u == n_tiles - 1) mma_commit(bar(B_O_FINAL));
+            for (int kk = 0; kk < NK / 16; ++kk) {
+                const uint64_t bd = sdesc(vf + kk * 2048, NK * 128, 1024);
+                mma_f16_ts(tmem + TM_O, tmem + TM_S + ub * 128 + 8 * kk, bd, ID_PV, (u > 0 || kk > 0));
+            }
+            mma_commit(bar(B_O_DONE));
+            mma_commit(bar(B_V_EMPTY + vb));
+            if (DUAL) mma_commit(bar(B_S_EMPTY + ub));
+            if (u == n_tiles - 1) mma_commit(bar(B_O_FINAL));
+            return true;
+        };
+        if (lane == 0) {
+            if (warp == 1) {
+                ok = mbar_wait(bar(B_Q_READY), 0);
+                fence_after();
+            }
+            if (!DUAL) {
+                // Q.K^T(t) then P.V(t - 1): Q.K^T of the next tile overlaps
+                // the softmax of this one
+                for (int t = 0; t <= n_tiles && ok; ++t) {
+                    if (t < n_tiles) ok = qk(t);
+                    if (ok && t >= 1) ok = pv(t - 1);
                 }
+            } else if (warp == 1) {
+                for (int t = 0; t < n_tiles && ok; ++t) ok = qk(t);
+            } else {
+                for (int u = 0; u < n_tiles && ok; ++u) ok = pv(u);
             }
             // nothing the tensor cores still run may outlive the TMEM allocation
             mma_commit(bar(B_MMA_IDLE));
             mbar_wait(bar(B_MMA_IDLE), 0);
         }
         __syncwarp();
-    } else if (is_converter(warp)) {
+    } else if (is_converter<DUAL>(warp)) {
         // ---------------------------------------------------------- V widening
         // 128 keys x 8 chunks of 16 E4M3 values -> two 64-dim blocks of
         // 128 x 128 B f16 (128B-swizzled): the MN-major B operand of P.V.
@@ -744,8 +779,13 @@ int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Attn
     if ((P.split_pages * P.page_size) % tc::NK) return FP8KV_ERR_UNSUPPORTED;
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
-    const void* kern = P.page_size == 32 ? (const void*)tc::attention_tc_kernel<32>
-                                         : (const void*)tc::attention_tc_kernel<64>;
+    // two issuing threads when no new tokens are appended in the kernel (the
+    // append encodes them in the converter warps, which then need all six)
+    const bool dual = P.k_new == nullptr;
+    const void* kern = P.page_size == 32 ? (dual ? (const void*)tc::attention_tc_kernel<32, true>
+                                                 : (const void*)tc::attention_tc_kernel<32, false>)
+                                         : (dual ? (const void*)tc::attention_tc_kernel<64, true>
+                                                 : (const void*)tc::attention_tc_kernel<64, false>);
     {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess) return FP8KV_ERR_CUDA;
@@ -761,8 +801,9 @@ int launch_attention_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Attn
     if (P.cluster > 1 && (P.cluster > 8 || P.cluster != P.num_splits)) return FP8KV_ERR_UNSUPPORTED;
     if (P.lpt_order && (RT > 1 || P.cluster > 1 || (int64_t)P.B * P.num_splits * P.Hkv > INT32_MAX))
         return FP8KV_ERR_UNSUPPORTED;
-    e = launch_pdl_cluster(P.page_size == 32 ? tc::attention_tc_kernel<32> : tc::attention_tc_kernel<64>, grid,
-                           dim3(tc::THREADS), tc::SMEM, s, P.cluster, tk, tv, P);
+    auto k = P.page_size == 32 ? (dual ? tc::attention_tc_kernel<32, true> : tc::attention_tc_kernel<32, false>)
+                               : (dual ? tc::attention_tc_kernel<64, true> : tc::attention_tc_kernel<64, false>);
+    e = launch_pdl_cluster(k, grid, dim3(tc::THREADS), tc::SMEM, s, P.cluster, tk, tv, P);
     return e == cudaSuccess ? FP8KV_OK : (cudaGetLastError(), FP8KV_ERR_CUDA);
 }
 
