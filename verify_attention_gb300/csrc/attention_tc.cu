@@ -60,9 +60,10 @@ constexpr int VBUFS = 2;                        // f16 V tiles
 constexpr int VBUF_BYTES = NK * 256;            // 32 KiB
 constexpr int XCH_BYTES = 3 * 2 * 128 * 4;      // [tile parity 0, parity 1, row sums][half][row]
 // Cluster combine: the partials a CTA receives for the rows it owns (row r
-// belongs to rank r mod C): C partitions x ceil(rows / C) slots, an f16 row
-// (O / l, 128 dims) and fp32 (max, sum) each; at most 136 slots for C <= 8.
-constexpr int RECV_SLOTS = 136;
+// belongs to rank r mod C): C partitions x S slots, S = ceil(rows / C)
+// rounded up to even (16-byte blocks of (max, sum)), an f16 row (O / l, 128
+// dims) and fp32 (max, sum) each; at most 143 slots for C <= 8.
+constexpr int RECV_SLOTS = 144;
 constexpr int RECV_BYTES = RECV_SLOTS * (256 + 8);
 constexpr int SMEM = STAGES * STG_BYTES + VBUFS * VBUF_BYTES + XCH_BYTES + RECV_BYTES + 1024 + 512;
 // epilogue: one staged half row (<= 256 B) per (half, row), padded against
@@ -93,8 +94,19 @@ enum {
     // whole phase behind
     B_PATCH = B_PAIR + 4,
     B_S_EMPTY = B_PATCH + 2,                    // per S buffer: P.V of the P over it done (DUAL)
-    B_COUNT = B_S_EMPTY + 2
+    B_RECV = B_S_EMPTY + 2,                     // cluster combine: every partition's partial rows arrived
+    B_COUNT = B_RECV + 1
 };
+
+// Named barrier 5 of the eight softmax warps that also ANDs `ok` over them.
+__device__ __forceinline__ bool softmax_warps_all(bool ok) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 5, 256, p; selp.u32 %0, 1, 0, q; }"
+                 : "=r"(r)
+                 : "r"((uint32_t)ok)
+                 : "memory");
+    return r != 0;
+}
 
 template <bool DUAL>
 __device__ __forceinline__ bool is_converter(int warp) { return warp == 2 || warp == 3 || (warp >= 12 && warp < 12 + conv_warps<DUAL>() - 2); }
@@ -152,6 +164,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         mbar_init(bar(B_PATCH), CONV_WARPS);
         mbar_init(bar(B_PATCH + 1), CONV_WARPS);
         for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
+        mbar_init(bar(B_RECV), 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -168,6 +181,9 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     __syncthreads();
     fence_after();
     const uint32_t tmem = *tmem_slot;
+    // cluster: every CTA has started and initialised its barriers before any
+    // partial is sent (arrive here, wait before the wait for the previous kernel)
+    if (P.cluster > 1) cluster_arrive_relaxed();
     if (warp == 1 && lane == 0 && !P.lpt_order) {
         // L2 prefetch of the block-table entries this partition will read,
         // located from a read of the sequence length made before the wait for
@@ -186,8 +202,17 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             for (uintptr_t a = a0; a < a1; a += 128)        // 128-byte lines, usually one
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
         }
+        // the query rows of this tile (one run of G heads per query m) to
+        // L2: where the previous kernel writes Q, its stores update these
+        // lines; where Q is older, the loads after the wait hit L2
+        for (int m = R0 / P.G; m <= (R0 + RL - 1) / P.G; ++m)
+            bulk_prefetch_l2(P.q + (((int64_t)b * P.M + m) * P.Hq + (int64_t)hk * P.G) * 128, P.G * 256);
     }
 
+    if (P.cluster > 1) {
+        __syncwarp();
+        cluster_wait();
+    }
     pdl_wait();
     bool have_work = true;
     if (P.lpt_order) {
@@ -217,6 +242,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         run = false;
     }
     if (split >= nsplit_b) run = false;
+    // cluster combine: S slots per partition (even), and the bytes this CTA
+    // receives, S rows + S (max, sum) pairs from each partition
+    const int cl_slots = P.cluster > 1 ? (((RL + P.cluster - 1) / P.cluster + 1) & ~1) : 0;
+    const bool cl_combine = P.cluster > 1 && seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits;
+    if (cl_combine && threadIdx.x == 0) mbar_expect_tx(bar(B_RECV), nsplit_b * cl_slots * (256 + 8));
     const int page_begin = first_page + split * P.split_pages;
     const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
     constexpr int PPT = NK / PS;                            // pages per tile
@@ -668,14 +698,15 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 4]) * f, __uint_as_float(ov[8 * v4 + 5]) * f),
                             pack_f16x2(__uint_as_float(ov[8 * v4 + 6]) * f, __uint_as_float(ov[8 * v4 + 7]) * f));
                     if (combine) {
-                        // straight into the receive area of the row's owner
-                        // (rank r mod C), slot r / C of this partition
+                        // staged by owner (rank r mod C), slot r / C: one
+                        // contiguous block per owner, sent below; 16-byte
+                        // chunk j of row r at chunk j ^ (r & 7), so that a
+                        // warp's 32 rows spread over all banks
                         if (r < RL) {
-                            const int C = P.cluster, slots = (RL + C - 1) / C;
-                            const uint32_t a =
-                                dsmem_addr(recv + (split_e * slots + r / C) * 256 + half * 128 + c * 2, r % C);
+                            uint8_t* row = stg + ((r % P.cluster) * cl_slots + r / P.cluster) * 256;
 #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4) st_dsmem_u32x4(a + 16 * v4, w[v4]);
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                *(uint4*)(row + (((half * 8 + c / 8 + v4) ^ (r & 7)) << 4)) = w[v4];
                         }
                     } else {
                         uint4* dst = (uint4*)(row_stage + c * 2);
@@ -696,11 +727,27 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             }
             if (r < RL && !direct && half == 0) {
                 if (combine) {
-                    const int C = P.cluster, slots = (RL + C - 1) / C;
-                    st_dsmem_f32x2(dsmem_addr(recv_ml + (split_e * slots + r / C) * 2, r % C), m_run, l_tot);
+                    float* cml = (float*)(stg + P.cluster * cl_slots * 256);
+                    *(float2*)(cml + ((r % P.cluster) * cl_slots + r / P.cluster) * 2) = make_float2(m_run, l_tot);
                 } else {
                     P.ws_ml[(row_idx * P.num_splits + split_e) * 2] = m_run;
                     P.ws_ml[(row_idx * P.num_splits + split_e) * 2 + 1] = l_tot;
+                }
+            }
+        }
+        if (cl_combine) {
+            // every softmax warp's staged rows, then one thread sends each
+            // owner its block of rows and its block of (max, sum), both
+            // completing on the owner's receive barrier
+            fence_proxy_async();
+            if (softmax_warps_all(ok) && warp == 4 && lane == 0) {
+                const float* cml = (const float*)(stg + P.cluster * cl_slots * 256);
+                for (int j = 0; j < P.cluster; ++j) {
+                    const uint32_t rb = dsmem_addr(&bars[B_RECV], j);
+                    bulk_copy_to_cluster(dsmem_addr(recv + split * cl_slots * 256, j),
+                                         smem_u32(stg + j * cl_slots * 256), cl_slots * 256, rb);
+                    bulk_copy_to_cluster(dsmem_addr(recv_ml + split * cl_slots * 2, j),
+                                         smem_u32(cml + j * cl_slots * 2), cl_slots * 8, rb);
                 }
             }
         }
@@ -709,53 +756,67 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     if (P.cluster > 1) {
         // ------------------------------------------------- cluster combine
         // The partitions of this (KV head, sequence) are the CTAs of one
-        // cluster (rank = partition).  Each has pushed its partial rows to
-        // their owners (row r to rank r mod C); after one cluster barrier
-        // every CTA combines the rows it owns from its own shared memory,
-        // one warp per row, lane l owning dims 4l..4l+3:
+        // cluster (rank = partition).  Each has staged its partial rows by
+        // owner (row r belongs to rank r mod C) and sent every owner its
+        // block with bulk copies that complete on the owner's receive
+        // barrier.  Once that barrier completes, a CTA combines the rows it
+        // owns from its own shared memory, 16 threads a row, each with 8
+        // dims, every thread reading all the partitions' (max, sum) itself:
         // O = v_scale * sum_p w_p O_p / sum_p w_p, w_p = 2^(m_p - m*) l_p.
-        // Nothing is read remotely, so no second barrier is needed.
+        // A split cluster barrier (arrive once this CTA has received, wait
+        // before exit) keeps each sender's staged blocks in place until
+        // every owner has them.
+        bool recv_ok = true;
+        if (cl_combine) recv_ok = mbar_wait(bar(B_RECV), 0);
         __syncwarp();
-        cluster_sync_all();
-        if (seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits) {
+        cluster_arrive_relaxed();
+        if (cl_combine && recv_ok) {
             const float vsc = P.v_scale[P.scale_stride * hk];
-            const int C = P.cluster, slots = (RL + C - 1) / C;
-            for (int k = warp; k < slots && split + C * k < RL; k += WARPS) {
+            const int C = P.cluster, slots = cl_slots;
+            for (int i = threadIdx.x; i < slots * 16; i += THREADS) {
+                const int k = i >> 4, ch = i & 15;
                 const int r = split + C * k;
-                uint2 v[8];
-#pragma unroll
-                for (int p = 0; p < 8; ++p)
-                    v[p] = p < nsplit_b ? *(const uint2*)(recv + (p * slots + k) * 256 + lane * 8) : make_uint2(0, 0);
-                float mp = -INFINITY, lp = 0.f;
-                if (lane < nsplit_b) {
-                    const float2 ml = *(const float2*)(recv_ml + (lane * slots + k) * 2);
-                    mp = ml.x;
-                    lp = ml.y;
-                }
-                float mstar = mp;
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) mstar = fmaxf(mstar, __shfl_xor_sync(0xffffffffu, mstar, off));
-                const float w = (mp == -INFINITY) ? 0.f : ex2(mp - mstar) * lp;
-                float lsum = w;
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (r >= RL) break;                         // r grows with i
+                float mp[8], lp[8];
+                float mstar = -INFINITY;
 #pragma unroll
                 for (int p = 0; p < 8; ++p) {
-                    const float wp = __shfl_sync(0xffffffffu, w, p);   // 0 past nsplit_b
-                    const float2 a = f16x2_to_f32x2(v[p].x), c2 = f16x2_to_f32x2(v[p].y);
-                    acc.x = fmaf(wp, a.x, acc.x);
-                    acc.y = fmaf(wp, a.y, acc.y);
-                    acc.z = fmaf(wp, c2.x, acc.z);
-                    acc.w = fmaf(wp, c2.y, acc.w);
+                    mp[p] = -INFINITY;
+                    lp[p] = 0.f;
+                    if (p < nsplit_b) {
+                        const float2 ml = *(const float2*)(recv_ml + (p * slots + k) * 2);
+                        mp[p] = ml.x;
+                        lp[p] = ml.y;
+                        mstar = fmaxf(mstar, ml.x);
+                    }
+                }
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                float lsum = 0.f;
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    if (p < nsplit_b) {
+                        const float w = (mp[p] == -INFINITY) ? 0.f : ex2(mp[p] - mstar) * lp[p];
+                        lsum += w;
+                        const uint4 o = *(const uint4*)(recv + (p * slots + k) * 256 + ((ch ^ (r & 7)) << 4));
+                        const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float2 f2 = f16x2_to_f32x2(ow[j]);
+                            acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
+                            acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
+                        }
+                    }
                 }
                 const float inv = vsc / lsum;
                 const int m = (R0 + r) / P.G;
                 const int64_t orow = ((int64_t)b * P.M + m) * P.Hq + hk * P.G + (R0 + r) % P.G;
-                *(uint2*)(P.out + orow * 128 + 4 * lane) =
-                    make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+                *(uint4*)(P.out + orow * 128 + 8 * ch) =
+                    make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                               pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
             }
         }
+        __syncwarp();
+        cluster_wait();
     }
 
     // ---------------------------------------------------------------- teardown

@@ -248,6 +248,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a
+// multiple of 16): a hint with no effect on any value read later.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tm) : "memory");
 }
@@ -299,28 +305,23 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* p, int rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
     return r;
 }
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint2 ld_dsmem_u32x2(uint32_t a) {
-    uint2 v;
-    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_dsmem_u32x4(uint32_t a, uint4 v) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from this CTA's shared memory to shared memory of a CTA of the cluster
+// (`dst`, `mbar`: addresses from dsmem_addr); the copy's bytes complete a
+// transaction on that CTA's mbarrier `mbar`.  The source must stay unchanged
+// until the receiver has seen the bytes arrive.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(mbar)
                  : "memory");
 }
-__device__ __forceinline__ void st_dsmem_f32x2(uint32_t a, float x, float y) {
-    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
+// Split cluster barrier, executed by every thread of every CTA of the
+// cluster (warp-aligned): arrive without ordering, then wait (acquire).
+// A fence.mbarrier_init before the arrive publishes barrier initialisation.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
-// Every thread of every CTA of the cluster: writes before it are visible to
-// reads after it anywhere in the cluster.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 int launch_status();                    // FP8KV_OK or FP8KV_ERR_CUDA after a launch
 int num_sms();                          // SM count of the current device
