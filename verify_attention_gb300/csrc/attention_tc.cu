@@ -419,9 +419,12 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             if (ok && t >= VBUFS) ok = mbar_wait(bar(B_V_EMPTY + vb), ((t / VBUFS) - 1) & 1);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const int k0 = k_begin + t * NK;
-            if (t >= app_t0 && t <= app_t1) {
-                // patch this tile's new rows (K and V, 128-byte swizzled rows of
-                // the staging buffer) with the appended tokens' codes
+            const bool patched = t >= app_t0 && t <= app_t1;
+            if (patched) {
+                // this tile's new rows of K (128-byte swizzled rows of the
+                // staging buffer) get the appended tokens' codes, for the
+                // Q.K^T of this tile; their V goes straight into the f16 tile
+                // below, so the widening waits for no other warp
                 uint8_t* kst = stg + s * STG_BYTES;
                 for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
                     uint2 kc = kc0, vc = vc0;
@@ -429,17 +432,16 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                     if (it != ct) app_item(it, kc, vc, pos, chunk);
                     const int r = pos - k0;
                     if (r < 0 || r >= NK) continue;
-                    const int off = r * 128 + ((((chunk >> 1) ^ r) & 7) << 4) + (chunk & 1) * 8;
-                    *(uint2*)(kst + off) = kc;
-                    *(uint2*)(kst + STG_K + off) = vc;
+                    *(uint2*)(kst + r * 128 + ((((chunk >> 1) ^ r) & 7) << 4) + (chunk & 1) * 8) = kc;
                 }
                 fence_proxy_async();                        // for the tensor cores' read of K
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_PATCH + (t - app_t0)));
-                // every converter warp's rows are in place before V is read
-                ok = mbar_wait(bar(B_PATCH + (t - app_t0)), 0);
-                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             }
+            // rows [nlo, nhi) of this tile hold appended tokens: the staged V
+            // bytes there may be old, so the widening below skips them
+            const int nlo = patched ? max(0, app_lo - k0) : 0;
+            const int nhi = patched ? min(NK, app_hi - k0) : 0;
             const int pages_here = min(PPT, n_pages - t * PPT);
             const int zlo = max(0, min(NK, lo0 - k0));
             const int zhi = max(0, min(min(NK, pages_here * PS), hi0 + 1 - k0));
@@ -460,6 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 const int i = ct + CONV_THREADS * u;
                 if (i >= NK * 8) break;
                 const int r = i >> 3, c = i & 7;
+                if (r >= nlo && r < nhi) continue;
                 uint4 lo, hi;
                 lo.x = e4m3x2_to_f16x2(code[u].x);
                 lo.y = e4m3x2_to_f16x2(code[u].x >> 16);
@@ -478,6 +481,24 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 } else {
                     *(uint4*)(blk + ((((c16 + 1) ^ r) & 7) << 4)) = hi;
                     *(uint4*)(blk + (((c16 ^ r) & 7) << 4)) = lo;
+                }
+            }
+            if (patched) {
+                // the appended tokens' V, widened from their codes: 8 values
+                // (half of a 16-byte f16 unit pair) per item
+                for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
+                    uint2 kc = kc0, vc = vc0;
+                    int pos = pos0, chunk = chunk0;
+                    if (it != ct) app_item(it, kc, vc, pos, chunk);
+                    const int r = pos - k0;
+                    if (r < 0 || r >= NK) continue;
+                    const int c = chunk >> 1;
+                    uint4 h;
+                    h.x = e4m3x2_to_f16x2(vc.x);
+                    h.y = e4m3x2_to_f16x2(vc.x >> 16);
+                    h.z = e4m3x2_to_f16x2(vc.y);
+                    h.w = e4m3x2_to_f16x2(vc.y >> 16);
+                    *(uint4*)(dst + (c >> 2) * (NK * 128) + r * 128 + ((((2 * (c & 3) + (chunk & 1)) ^ r) & 7) << 4)) = h;
                 }
             }
             fence_proxy_async();
@@ -579,9 +600,16 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 tmem_ld_x64(scol, sv);
                 tmem_wait_ld();
                 if ((k0 + 63 > pmin) || (k0 < lomax)) {
+                    // this row's visible columns of the half, [jlo, jhi), as
+                    // a bit mask: one bit test and select per column
+                    const int jlo = max(0, lo_r - k0), jhi = min(64, p_r - k0 + 1);
+                    const uint64_t below_hi = jhi <= 0 ? 0ull : (jhi >= 64 ? ~0ull : (1ull << jhi) - 1);
+                    const uint64_t below_lo = jlo >= 64 ? ~0ull : (1ull << jlo) - 1;
+                    const uint64_t vis = below_hi & ~below_lo;
+                    const uint32_t vis_lo = (uint32_t)vis, vis_hi = (uint32_t)(vis >> 32);
 #pragma unroll
                     for (int j = 0; j < 64; ++j)
-                        if (k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
+                        sv[j] = (((j < 32 ? vis_lo : vis_hi) >> (j & 31)) & 1u) ? sv[j] : 0xff800000u;   // -inf
                 }
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
