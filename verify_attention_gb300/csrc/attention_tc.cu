@@ -214,6 +214,18 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         cluster_wait();
     }
     pdl_wait();
+    // Converter thread ct's first append item is query m = ct / 16 whenever
+    // the partition starts at or before the first new token (the usual case):
+    // its K and V rows are loaded now, beside the sequence length, instead of
+    // a round trip after it
+    uint4 spec_k = make_uint4(0, 0, 0, 0), spec_v = make_uint4(0, 0, 0, 0);
+    const int ct_spec = converter_index(warp) * 32 + lane;
+    const bool spec = P.k_new != nullptr && !P.lpt_order && is_converter<DUAL>(warp) && ct_spec < P.M * 16;
+    if (spec) {
+        const int64_t src = (((int64_t)b * P.M + (ct_spec >> 4)) * P.Hkv + hk) * 16 + (ct_spec & 15);
+        spec_k = ((const uint4*)P.k_new)[src];
+        spec_v = ((const uint4*)P.v_new)[src];
+    }
     bool have_work = true;
     if (P.lpt_order) {
         // CTA i: KV head i mod Hkv of the slot of rank i / Hkv, longest first
@@ -385,33 +397,21 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             chunk = it & 15;
             const int m = pos - (L - P.M);
             const int64_t src = (((int64_t)b * P.M + m) * P.Hkv + hk) * 16 + chunk;
-            kc = e4m3_encode8(((const uint4*)P.k_new)[src], ksc);
-            vc = e4m3_encode8(((const uint4*)P.v_new)[src], vsc);
+            const bool have = spec && it == ct && app_lo == L - P.M;   // loaded before the length
+            kc = e4m3_encode8(have ? spec_k : ((const uint4*)P.k_new)[src], ksc);
+            vc = e4m3_encode8(have ? spec_v : ((const uint4*)P.v_new)[src], vsc);
         };
-        // ---------------------------------------------------- append insert
-        // the new tokens of this head into the cache (the cache-insert
-        // encoding); the staged tiles get the same bytes below (each thread
-        // keeps its first item's codes for that)
+        // ----------------------------------------------------- append codes
+        // this thread's first item of the new tokens in the cache-insert
+        // encoding: the staged tile that holds it is patched with these codes
+        // in the loop below, and the cache is written after that loop (the
+        // block-table read for the token's page stays off the path to the
+        // first Q.K^T; it is issued here and used there)
         uint2 kc0 = make_uint2(0, 0), vc0 = make_uint2(0, 0);
-        int pos0 = -1, chunk0 = 0;
-        for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
-            uint2 kc, vc;
-            int pos, chunk;
-            app_item(it, kc, vc, pos, chunk);
-            if (it == ct) {
-                kc0 = kc;
-                vc0 = vc;
-                pos0 = pos;
-                chunk0 = chunk;
-            }
-            const int page = P.block_table[(int64_t)b * P.mpps + pos / PS];
-            if (page < 0 || page >= P.num_pages) {
-                if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
-                continue;
-            }
-            const int64_t dst = (((int64_t)page * P.Hkv + hk) * PS + pos % PS) * 128 + chunk * 8;
-            *(uint2*)(P.k_cache + dst) = kc;
-            *(uint2*)(P.v_cache + dst) = vc;
+        int pos0 = -1, chunk0 = 0, page0 = -1;
+        if (ct < n_app * 16) {
+            app_item(ct, kc0, vc0, pos0, chunk0);
+            page0 = P.block_table[(int64_t)b * P.mpps + pos0 / PS];
         }
         for (int t = 0; t < n_tiles; ++t) {
             const int s = t % STAGES, vb = t % VBUFS;
@@ -508,6 +508,23 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 mbar_arrive(bar(B_V_FULL + vb));
             }
         }
+        // ---------------------------------------------------- append insert
+        // the new tokens of this head into the cache
+        for (int it = ct; it < n_app * 16; it += CONV_THREADS) {
+            uint2 kc = kc0, vc = vc0;
+            int pos = pos0, chunk = chunk0, page = page0;
+            if (it != ct) {
+                app_item(it, kc, vc, pos, chunk);
+                page = P.block_table[(int64_t)b * P.mpps + pos / PS];
+            }
+            if (page < 0 || page >= P.num_pages) {
+                if (chunk == 0) flag(FP8KV_DEV_BAD_SLOT);
+                continue;
+            }
+            const int64_t dst = (((int64_t)page * P.Hkv + hk) * PS + pos % PS) * 128 + chunk * 8;
+            *(uint2*)(P.k_cache + dst) = kc;
+            *(uint2*)(P.v_cache + dst) = vc;
+        }
     } else {
         // ------------------------------------------------------------ softmax
         const int wq = warp & 3, half = (warp - 4) >> 2;
@@ -581,11 +598,13 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_Q_READY));
 
-        int pmin = p_r, lomax = lo_r;
+        int pmin = p_r, lomax = lo_r, pmax = p_r, lomin = lo_r;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, off));
             lomax = max(lomax, __shfl_xor_sync(0xffffffffu, lomax, off));
+            pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, off));
+            lomin = min(lomin, __shfl_xor_sync(0xffffffffu, lomin, off));
         }
         float m_run = -INFINITY, l_run = 0.f;               // l_run: this half's columns only
         for (int t = 0; t < n_tiles; ++t) {
@@ -596,30 +615,37 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             if (active) {
                 const uint32_t scol = lane_base + TM_S + sb * 128 + 64 * half;
                 const int k0 = k_begin + t * NK + 64 * half;   // first key of this half
+                // no row of this warp sees any key of the half (the end of
+                // the last tile, the start of a window): its P is zero
+                const bool dead = (k0 > pmax) || (k0 + 63 < lomin);
                 uint32_t sv[64];
-                tmem_ld_x64(scol, sv);
-                tmem_wait_ld();
-                if ((k0 + 63 > pmin) || (k0 < lomax)) {
-                    // this row's visible columns of the half, [jlo, jhi), as
-                    // a bit mask: one bit test and select per column
-                    const int jlo = max(0, lo_r - k0), jhi = min(64, p_r - k0 + 1);
-                    const uint64_t below_hi = jhi <= 0 ? 0ull : (jhi >= 64 ? ~0ull : (1ull << jhi) - 1);
-                    const uint64_t below_lo = jlo >= 64 ? ~0ull : (1ull << jlo) - 1;
-                    const uint64_t vis = below_hi & ~below_lo;
-                    const uint32_t vis_lo = (uint32_t)vis, vis_hi = (uint32_t)(vis >> 32);
+                float hmax = -INFINITY;
+                if (!dead) {
+                    tmem_ld_x64(scol, sv);
+                    tmem_wait_ld();
+                    if ((k0 + 63 > pmin) || (k0 < lomax)) {
+                        // this row's visible columns of the half, [jlo, jhi), as
+                        // a bit mask: one bit test and select per column
+                        const int jlo = max(0, lo_r - k0), jhi = min(64, p_r - k0 + 1);
+                        const uint64_t below_hi = jhi <= 0 ? 0ull : (jhi >= 64 ? ~0ull : (1ull << jhi) - 1);
+                        const uint64_t below_lo = jlo >= 64 ? ~0ull : (1ull << jlo) - 1;
+                        const uint64_t vis = below_hi & ~below_lo;
+                        const uint32_t vis_lo = (uint32_t)vis, vis_hi = (uint32_t)(vis >> 32);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j)
-                        sv[j] = (((j < 32 ? vis_lo : vis_hi) >> (j & 31)) & 1u) ? sv[j] : 0xff800000u;   // -inf
-                }
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        for (int j = 0; j < 64; ++j)
+                            sv[j] = (((j < 32 ? vis_lo : vis_hi) >> (j & 31)) & 1u) ? sv[j] : 0xff800000u;   // -inf
+                    }
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    m4[0] = fmaxf(m4[0], __uint_as_float(sv[j]));
-                    m4[1] = fmaxf(m4[1], __uint_as_float(sv[j + 1]));
-                    m4[2] = fmaxf(m4[2], __uint_as_float(sv[j + 2]));
-                    m4[3] = fmaxf(m4[3], __uint_as_float(sv[j + 3]));
+                    for (int j = 0; j < 64; j += 4) {
+                        m4[0] = fmaxf(m4[0], __uint_as_float(sv[j]));
+                        m4[1] = fmaxf(m4[1], __uint_as_float(sv[j + 1]));
+                        m4[2] = fmaxf(m4[2], __uint_as_float(sv[j + 2]));
+                        m4[3] = fmaxf(m4[3], __uint_as_float(sv[j + 3]));
+                    }
+                    hmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                 }
-                xch[(sb * 2 + half) * 128 + r] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                xch[(sb * 2 + half) * 128 + r] = hmax;
                 // exchange with the partner warp (bounded wait, phase t of the pair barrier)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_PAIR + wq));
@@ -655,13 +681,18 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 // both halves' S reads are complete (pair barrier above)
                 float sum0 = 0.f, sum1 = 0.f;
                 uint32_t pw[32];
+                if (!dead) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sv[2 * j]), mult, neg));
-                    const float p1 = ex2(fmaf(__uint_as_float(sv[2 * j + 1]), mult, neg));
-                    sum0 += p0;
-                    sum1 += p1;
-                    pw[j] = pack_f16x2(p0, p1);
+                    for (int j = 0; j < 32; ++j) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * j]), mult, neg));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * j + 1]), mult, neg));
+                        sum0 += p0;
+                        sum1 += p1;
+                        pw[j] = pack_f16x2(p0, p1);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) pw[j] = 0u;
                 }
                 tmem_st_x32(lane_base + TM_S + sb * 128 + 32 * half, pw);
                 l_run += sum0 + sum1;
