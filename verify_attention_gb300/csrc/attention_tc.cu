@@ -202,11 +202,6 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             for (uintptr_t a = a0; a < a1; a += 128)        // 128-byte lines, usually one
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(a) : "memory");
         }
-        // the query rows of this tile (one run of G heads per query m) to
-        // L2: where the previous kernel writes Q, its stores update these
-        // lines; where Q is older, the loads after the wait hit L2
-        for (int m = R0 / P.G; m <= (R0 + RL - 1) / P.G; ++m)
-            bulk_prefetch_l2(P.q + (((int64_t)b * P.M + m) * P.Hq + (int64_t)hk * P.G) * 128, P.G * 256);
     }
 
     if (P.cluster > 1) {
@@ -220,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     // a round trip after it
     uint4 spec_k = make_uint4(0, 0, 0, 0), spec_v = make_uint4(0, 0, 0, 0);
     const int ct_spec = converter_index(warp) * 32 + lane;
-    const bool spec = P.k_new != nullptr && !P.lpt_order && is_converter<DUAL>(warp) && ct_spec < P.M * 16;
+    const bool spec = !DUAL && P.k_new != nullptr && !P.lpt_order && is_converter<DUAL>(warp) && ct_spec < P.M * 16;
     if (spec) {
         const int64_t src = (((int64_t)b * P.M + (ct_spec >> 4)) * P.Hkv + hk) * 16 + (ct_spec & 15);
         spec_k = ((const uint4*)P.k_new)[src];
@@ -255,10 +250,11 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     }
     if (split >= nsplit_b) run = false;
     // cluster combine: S slots per partition (even), and the bytes this CTA
-    // receives, S rows + S (max, sum) pairs from each partition
-    const int cl_slots = P.cluster > 1 ? (((RL + P.cluster - 1) / P.cluster + 1) & ~1) : 0;
-    const bool cl_combine = P.cluster > 1 && seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits;
-    if (cl_combine && threadIdx.x == 0) mbar_expect_tx(bar(B_RECV), nsplit_b * cl_slots * (256 + 8));
+    // receives, S rows + S (max, sum) pairs from each partition (both are
+    // recomputed where they are used, rather than held through the tile loop)
+    auto cl_slots_of = [&]() { return ((RL + P.cluster - 1) / P.cluster + 1) & ~1; };
+    auto cl_combine_of = [&]() { return P.cluster > 1 && seq_ok && nsplit_b > 1 && nsplit_b <= P.num_splits; };
+    if (cl_combine_of() && threadIdx.x == 0) mbar_expect_tx(bar(B_RECV), nsplit_b * cl_slots_of() * (256 + 8));
     const int page_begin = first_page + split * P.split_pages;
     const int n_pages = min(P.split_pages, last_page + 1 - page_begin);
     constexpr int PPT = NK / PS;                            // pages per tile
@@ -462,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 const int i = ct + CONV_THREADS * u;
                 if (i >= NK * 8) break;
                 const int r = i >> 3, c = i & 7;
-                if (r >= nlo && r < nhi) continue;
+                if (!DUAL && r >= nlo && r < nhi) continue;
                 uint4 lo, hi;
                 lo.x = e4m3x2_to_f16x2(code[u].x);
                 lo.y = e4m3x2_to_f16x2(code[u].x >> 16);
@@ -617,13 +613,17 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 const int k0 = k_begin + t * NK + 64 * half;   // first key of this half
                 // no row of this warp sees any key of the half (the end of
                 // the last tile, the start of a window): its P is zero
-                const bool dead = (k0 > pmax) || (k0 + 63 < lomin);
+                const bool dead = !DUAL && ((k0 > pmax) || (k0 + 63 < lomin));
                 uint32_t sv[64];
                 float hmax = -INFINITY;
                 if (!dead) {
                     tmem_ld_x64(scol, sv);
                     tmem_wait_ld();
-                    if ((k0 + 63 > pmin) || (k0 < lomax)) {
+                    if (DUAL && ((k0 + 63 > pmin) || (k0 < lomax))) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j)
+                            if (k0 + j > p_r || k0 + j < lo_r) sv[j] = 0xff800000u;   // -inf
+                    } else if ((k0 + 63 > pmin) || (k0 < lomax)) {
                         // this row's visible columns of the half, [jlo, jhi), as
                         // a bit mask: one bit test and select per column
                         const int jlo = max(0, lo_r - k0), jhi = min(64, p_r - k0 + 1);
@@ -717,6 +717,7 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
             const float l_tot = xch[4 * 128 + r] + xch[5 * 128 + r];
             const bool direct = nsplit_b == 1;
             const bool combine = !direct && P.cluster > 1;  // partial stays in shared memory
+            const int cl_slots = cl_slots_of();
             // the partition index, read again here rather than held through
             // the tile loop
             const int split_e =
@@ -794,7 +795,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
                 }
             }
         }
-        if (cl_combine) {
+        if (cl_combine_of()) {
+            const int cl_slots = cl_slots_of();
             // every softmax warp's staged rows, then one thread sends each
             // owner its block of rows and its block of (max, sum), both
             // completing on the owner's receive barrier
@@ -826,6 +828,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
         // before exit) keeps each sender's staged blocks in place until
         // every owner has them.
         bool recv_ok = true;
+        const bool cl_combine = cl_combine_of();
+        const int cl_slots = cl_slots_of();
         if (cl_combine) recv_ok = mbar_wait(bar(B_RECV), 0);
         __syncwarp();
         cluster_arrive_relaxed();
