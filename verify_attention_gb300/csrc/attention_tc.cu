@@ -262,7 +262,8 @@ __global__ void __launch_bounds__(THREADS, 1) attention_tc_kernel(const __grid_c
     const int k_begin = page_begin * PS;
     // append: new tokens at positions [L - M, L) that fall in this partition
     const int app_lo = max(L - P.M, k_begin), app_hi = min(L, k_begin + n_pages * PS);
-    const bool appends = P.k_new != nullptr && run && app_lo < app_hi;
+    // (the two-issuer form serves only calls without appended tokens)
+    const bool appends = !DUAL && P.k_new != nullptr && run && app_lo < app_hi;
     // Appended tokens are written to the cache in global memory and, so that
     // no load has to wait for that write, also patched into the staged copy of
     // the tile that holds them (which may have been loaded with the old bytes):
