@@ -287,6 +287,8 @@ def test_empty_batch_launches_nothing():
     ([700], 12, 32, None, 0),            # one sequence: one wave of partitions + reduce
     ([640], 12, 32, 512, 0),             # one sequence, sliding: cluster combine
     ([1000], 12, 32, None, 128),         # 8-CTA cluster, new tokens straddling a tile edge
+    ([900], 12, 32, None, 128),          # 8-CTA cluster, new tokens in the last two partitions
+    ([1163], 12, 32, 512, 0),            # sliding 5-CTA cluster, new tokens in the last two partitions
     ([300, 1000, 77], 12, 64, None, 0),  # batch, tensor-memory kernel
     ([130, 33], 12, 32, 40, 64),         # mma.sync kernel with the append kernel
     ([500, 33], 1, 64, None, 0),         # decode kernel with the append kernel
